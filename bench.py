@@ -1,0 +1,415 @@
+"""Benchmark: tree-verified node-tokens/s through one GDN layer on GB300.
+
+One step = one pass of the whole hot path over one batch of draft trees:
+tree descriptor (ancestor masks, depths) -> fused verify (every node's output)
+-> delayed commit (new state along each request's accepted path).
+
+Default workload: batch 64, every tree 128 nodes (random, depth <= 16),
+16 key / 32 value heads, d_k = d_v = 128, bf16 q/k/v, fp32 g/beta/state.
+Inputs are seeded synthetic data resident in HBM; L2 is flushed (256 MiB
+write) between timed steps; each step is timed with CUDA events on the
+launching stream.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the path has no cross-request exchange): value = all ranks' node-tokens /
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_net_gb300 import workloads as W  # noqa: E402
+
+METRIC = "tree-verified node-tokens/s per GDN layer (1 GB300); HBM GB/s and % roofline"
+UNIT = "node-tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
+    "verify_simt": ["gated_delta_net_gb300/csrc/verify_simt.cu"],
+}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic byte and FLOP counts (each input byte once, each output byte once)
+# ----------------------------------------------------------------------------
+
+def verify_bytes(tb) -> int:
+    esz = 2 if tb.qkv_dtype == "bf16" else 4
+    osz = esz
+    total = 4 * (tb.batch + 1)
+    for n in tb.sizes():
+        n = int(n)
+        words = max(1, (tb.max_nodes + 31) // 32)
+        total += tb.n_v_heads * tb.d_v * tb.d_k * 4
+        total += n * (2 * tb.n_k_heads * tb.d_k * esz + tb.n_v_heads * tb.d_v * esz
+                      + tb.n_v_heads * 8 + tb.n_v_heads * tb.d_v * osz + 4 + 4 + 4 * words)
+    return total
+
+
+def commit_bytes(tb) -> int:
+    esz = 2 if tb.qkv_dtype == "bf16" else 4
+    L = len(tb.path_idx)
+    return (2 * tb.batch * tb.n_v_heads * tb.d_v * tb.d_k * 4
+            + L * (tb.n_k_heads * tb.d_k * esz + tb.n_v_heads * tb.d_v * esz + tb.n_v_heads * 8 + 8)
+            + 8 * (tb.batch + 1))
+
+
+def desc_bytes(tb) -> int:
+    words = max(1, (tb.max_nodes + 31) // 32)
+    return tb.total_nodes * (4 + 4 + 4 * words) + 4 * (tb.batch + 1)
+
+
+def verify_flops(tb) -> int:
+    """Per (request, value head): 4 N d^2 for the two S0 contractions plus
+    2 d (4 P - 2 N) for the ancestor-pair terms (P = sum of path lengths)."""
+    total = 0
+    d = tb.d_k
+    for b in range(tb.batch):
+        lo, hi = tb.node_offsets[b], tb.node_offsets[b + 1]
+        par = tb.parent[lo:hi]
+        depth = np.zeros(hi - lo, np.int64)
+        for i in range(hi - lo):
+            depth[i] = 1 if par[i] < 0 else depth[par[i]] + 1
+        n, P = int(hi - lo), int(depth.sum())
+        total += tb.n_v_heads * (4 * n * d * d + 2 * d * (4 * P - 2 * n))
+    return total
+
+
+def source_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(tb, seconds: float, seed: int = 0):
+    """Time the float64 oracle on a random sample of (request, value head, node)
+    outputs sized to take about `seconds`; returns (node-tokens/s, threads, desc)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    sizes = tb.sizes()
+
+    def draw(m):
+        bs = rng.integers(0, tb.batch, m)
+        return [(int(b), int(rng.integers(0, tb.n_v_heads)), int(rng.integers(0, max(1, sizes[b]))))
+                for b in bs]
+
+    m = 4 * threads
+    t0 = time.perf_counter()
+    oracle.verify_selected(tb, draw(m), threads)
+    dt = time.perf_counter() - t0
+    m = int(min(max(m * seconds / max(dt, 1e-3), m), 2_000_000))
+    sel = draw(m)
+    t0 = time.perf_counter()
+    oracle.verify_selected(tb, sel, threads)
+    dt = time.perf_counter() - t0
+    value = (m / tb.n_v_heads) / dt
+    desc = (f"{m} random (request, value head, node) outputs of the workload, each a "
+            f"sequential float64 path walk from S0; node-tokens = outputs / {tb.n_v_heads} heads")
+    return value, threads, desc, dt
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from gated_delta_net_gb300 import binding as gb
+    from gated_delta_net_gb300 import build as gbuild
+
+    gbuild.build()
+    gb.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    d = gb.upload(tb, device=dev)
+    T = tb.total_nodes
+    words = max(1, (tb.max_nodes + 31) // 32)
+    mask = torch.empty((T, words), dtype=torch.int32, device=dev)
+    depth = torch.empty(T, dtype=torch.int32, device=dev)
+    o = torch.empty((T, tb.n_v_heads, tb.d_v), dtype=torch.bfloat16, device=dev)
+    S_new = torch.empty_like(d["S0"])
+    status = gb.new_status(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes, mask, depth, words,
+                               status, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                           d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                           out=o, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                           d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes, out=S_new,
+                           dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    gb.check_status(status)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    with ClockSampler(gpu_id) as clk:
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            step((e[2], e[3]))
+            e[1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    gb.check_status(status)
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    verify_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    nodes = T * world
+    value = nodes * args.steps / total_s
+    ms_per_step = total_s * 1e3 / args.steps
+
+    # end to end through the public API: pinned host inputs in, o and S_new out
+    h = gb.upload(tb, pin=True)
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    S_h = torch.empty(S_new.shape, dtype=S_new.dtype, pin_memory=True)
+    keys = ["q", "k", "v", "g", "beta", "S0", "node_offsets", "parent", "path_offsets", "path_idx"]
+    h2d = sum(h[k].numel() * h[k].element_size() for k in keys)
+    d2h = o.numel() * o.element_size() + S_new.numel() * S_new.element_size()
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_ev = []
+    for it in range(e2e_steps + 1):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in keys:
+            d[k].copy_(h[k], non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_new, non_blocking=True)
+        e1.record(stream)
+        if it > 0:
+            e2e_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = nodes * e2e_steps / e2e_s
+
+    if rank != 0:
+        return None
+    hbm_gbs, bf16_tf, peak_kind = load_peaks()
+    vbytes = verify_bytes(tb)
+    v_s = statistics.mean(verify_ms) / 1e3
+    achieved = vbytes / v_s / 1e9
+    kernel = dominant_kernel(tb)
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        ent = tr.get(kernel)
+        if ent and ent.get("source_sha") == source_sha(KERNEL_SOURCES[kernel]) and \
+                ent.get("workload") == tb.name:
+            traffic = ent.get("dram_bytes_per_launch")
+    cpu_v, cpu_threads, cpu_desc, _ = oracle_sample(tb, args.cpu_seconds)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
+                   "tree": "random parent over nodes of depth < 16 (depth <= 16)",
+                   "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
+                   "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
+                   "step": "build_desc + verify + commit",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": vbytes,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "verify_only": {"us_per_launch": v_s * 1e6, "node_tokens_per_s": T / v_s,
+                        "tflops": verify_flops(tb) / v_s / 1e12},
+        "step_bytes": {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)},
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
+                         "sample": cpu_desc},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
+def dominant_kernel(tb) -> str:
+    """The verify kernel the library dispatches to (rule of include/gdn_tree.h)."""
+    if (TC_READY and tb.qkv_dtype == "bf16" and tb.d_k == 128 and tb.d_v == 128
+            and tb.max_nodes <= 128 and 1 <= tb.max_depth_bound <= 16):
+        return "verify_tc"
+    return "verify_simt"
+
+
+TC_READY = False
+
+
+def run_reference(args, rank, world):
+    """The float64 CPU oracle on the same workload and metric (rank 0 only)."""
+    if rank != 0:
+        return None
+    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    vals, ts = [], []
+    import oracle
+    oracle.build()
+    for i in range(args.warmup + args.steps):
+        v, threads, desc, dt = oracle_sample(tb, args.ref_seconds, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+            ts.append(dt)
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(ts),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
+                   "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
+                   "d_v": tb.d_v, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--tree-size", type=int, default=128)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,117 @@
+// api.cu -- host side of the C ABI: argument checks, kernel choice, error text.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+
+#include "internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+bool valid_dtype(int t) { return t == GDN_F32 || t == GDN_BF16; }
+
+int check_common(int batch, int hk, int hv, int dk, int dv, int max_nodes) {
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (hk < 1 || hv < 1) return fail(GDN_ERR_INVALID_ARG, "head counts must be >= 1");
+    if (hv % hk) return fail(GDN_ERR_INVALID_ARG, "n_v_heads %d not a multiple of n_k_heads %d", hv, hk);
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(GDN_ERR_UNSUPPORTED, "d_k=%d d_v=%d: supported sizes are 16, 32, 64, 128", dk, dv);
+    if (max_nodes < 1) return fail(GDN_ERR_INVALID_ARG, "max_nodes %d < 1", max_nodes);
+    if (max_nodes > gdn::kMaxNodes)
+        return fail(GDN_ERR_UNSUPPORTED, "max_nodes %d > %d", max_nodes, gdn::kMaxNodes);
+    return GDN_OK;
+}
+
+int check_verify(const gdn_verify_args *a) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
+    int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
+    if (st) return st;
+    if (!valid_dtype(a->qkv_dtype) || !valid_dtype(a->out_dtype))
+        return fail(GDN_ERR_UNSUPPORTED, "unknown dtype (qkv %d, out %d)", a->qkv_dtype, a->out_dtype);
+    if (a->max_depth < 0) return fail(GDN_ERR_INVALID_ARG, "max_depth %d < 0", a->max_depth);
+    if (!std::isfinite(a->scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    if (a->batch == 0) return GDN_OK;
+    if (!a->node_offsets || !a->q || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
+        !a->anc_mask || !a->depth || !a->o)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (a->mask_words < (a->max_nodes + 31) / 32 || a->mask_words > gdn::kMaxWords)
+        return fail(GDN_ERR_INVALID_ARG, "mask_words %d must be in [%d, %d]", a->mask_words,
+                    (a->max_nodes + 31) / 32, gdn::kMaxWords);
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_last_error(void) { return g_err; }
+
+int gdn_tree_version(void) { return 100; }
+
+int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offsets, int32_t batch,
+                        int32_t max_nodes, uint32_t *anc_mask, int32_t mask_words,
+                        int32_t *depth, int32_t *dev_status, void *stream) {
+    g_err[0] = 0;
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (max_nodes < 1) return fail(GDN_ERR_INVALID_ARG, "max_nodes %d < 1", max_nodes);
+    if (max_nodes > gdn::kMaxNodes)
+        return fail(GDN_ERR_UNSUPPORTED, "max_nodes %d > %d", max_nodes, gdn::kMaxNodes);
+    if (mask_words < (max_nodes + 31) / 32 || mask_words > gdn::kMaxWords)
+        return fail(GDN_ERR_INVALID_ARG, "mask_words %d must be in [%d, %d]", mask_words,
+                    (max_nodes + 31) / 32, gdn::kMaxWords);
+    if (batch == 0) return GDN_OK;
+    if (!parent || !node_offsets || !anc_mask || !depth)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    cudaError_t e = gdn::launch_build_desc(parent, node_offsets, batch, max_nodes, anc_mask,
+                                           mask_words, depth, dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "build_desc launch");
+}
+
+int gdn_tree_verify(const gdn_verify_args *a, void *stream) {
+    g_err[0] = 0;
+    int st = check_verify(a);
+    if (st || a->batch == 0) return st;
+    cudaError_t e = gdn::verify_tc_supported(*a)
+                        ? gdn::launch_verify_tc(*a, (cudaStream_t)stream)
+                        : gdn::launch_verify_simt(*a, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "verify launch");
+}
+
+int gdn_tree_verify_branches(const gdn_verify_args *a, void *stream) {
+    g_err[0] = 0;
+    int st = check_verify(a);
+    if (st || a->batch == 0) return st;
+    cudaError_t e = gdn::launch_verify_branches(*a, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "verify_branches launch");
+}
+
+int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
+    g_err[0] = 0;
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
+    int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
+    if (st) return st;
+    if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
+    if (a->batch == 0) return GDN_OK;
+    if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
+        !a->path_offsets || !a->path_idx || !a->S_new)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    cudaError_t e = gdn::launch_commit_simt(*a, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// internal.cuh -- shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_tree.h"
+
+namespace gdn {
+
+constexpr int kMaxNodes = 256;
+constexpr int kMaxWords = kMaxNodes / 32;
+
+__device__ __forceinline__ float load_f(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_f(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_f(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_f(__nv_bfloat16 *p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void flag(int32_t *status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// ---------------------------------------------------------------------------
+// launchers (one per translation unit); each returns a cudaError_t
+// ---------------------------------------------------------------------------
+cudaError_t launch_build_desc(const int32_t *parent, const int32_t *node_offsets, int batch,
+                              int max_nodes, uint32_t *anc_mask, int mask_words,
+                              int32_t *depth, int32_t *dev_status, cudaStream_t stream);
+
+cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream);
+cudaError_t launch_verify_branches(const gdn_verify_args &a, cudaStream_t stream);
+cudaError_t launch_commit_simt(const gdn_commit_args &a, cudaStream_t stream);
+
+// tcgen05/TMA fast path; returns cudaErrorNotSupported when the shape is not covered
+bool verify_tc_supported(const gdn_verify_args &a);
+cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream);
+
+}  // namespace gdn

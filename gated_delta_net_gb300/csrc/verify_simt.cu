@@ -1,0 +1,258 @@
+// verify_simt.cu -- general tree verification kernel (any dtype, any d, any depth).
+//
+// "Trees from Marginals" (gist.science Technical Summary, section 3
+// "Rollback-Free Tree Verification for GDN"): the outputs of every node of a
+// topologically sorted draft tree come from one triangular solve,
+//     (I + X) U = beta * (V - exp(gamma) * K S0^T),
+//     O = scale * (exp(gamma) * Q S0^T + Y U),
+// where X and Y only couple a node to its ancestors.  Because row i of X has
+// non-zeros only on i's strict ancestors, the solve runs level by level: all
+// nodes at one depth are independent once the shallower levels are done.
+//
+// One block per (d_v slab of 32 columns, value head, request); 8 warps.
+//   phase 0: tree metadata, gamma (sum of g along each path), depth buckets;
+//   phase 1: per node, W = S0 k, Z = S0 q for the slab, R = beta (v - e^gamma W);
+//   phase 2: per depth level, per node (one warp): dot products with each
+//            ancestor's key, forward substitution for u_i, then o_i.
+// Only a node's ancestors are ever read, so a non-finite input on one branch
+// cannot reach another branch's outputs.  Everything accumulates in fp32.
+#include "internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct SimtParams {
+    int hk_n, hv_n, dv, max_nodes, sw;
+    float scale;
+    const int32_t *offsets, *parent, *depth;
+    const void *q, *k, *v;
+    const float *g, *beta, *S0;
+    void *o;
+    int32_t *status;
+};
+
+struct SmemLayout {
+    int s0, ub, zb, gam, gl, bet, kq;  // float offsets
+    int par, dep, order, cnt, start;   // int offsets (after the floats)
+    int floats, ints;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int nm, int sw, int dk) {
+    SmemLayout L;
+    int f = 0;
+    L.s0 = f;  f += sw * (dk + 1);
+    L.ub = f;  f += nm * sw;
+    L.zb = f;  f += nm * sw;
+    L.gam = f; f += nm;
+    L.gl = f;  f += nm;
+    L.bet = f; f += nm;
+    L.kq = f;  f += kWarps * 2 * dk;
+    L.floats = f;
+    int i = 0;
+    L.par = i;   i += nm;
+    L.dep = i;   i += nm;
+    L.order = i; i += nm;
+    L.cnt = i;   i += nm + 2;
+    L.start = i; i += nm + 2;
+    L.ints = i;
+    return L;
+}
+
+template <typename Tin, typename Tout, int DK>
+__global__ void __launch_bounds__(kThreads)
+verify_simt_kernel(SimtParams p) {
+    constexpr int EPL = (DK + 31) / 32;  // key elements per lane
+    extern __shared__ float smem[];
+    const int nm = p.max_nodes, SW = p.sw;
+    const SmemLayout L = smem_layout(nm, SW, DK);
+    float *S0s = smem + L.s0, *Ub = smem + L.ub, *Zb = smem + L.zb;
+    float *gam = smem + L.gam, *gl = smem + L.gl, *bet = smem + L.bet;
+    int *ism = reinterpret_cast<int *>(smem + L.floats);
+    int *par = ism + L.par, *dep = ism + L.dep, *order = ism + L.order;
+    int *cnt = ism + L.cnt, *start = ism + L.start;
+    __shared__ int s_maxd;
+
+    const int nslab = p.dv / p.sw;
+    const int slab = blockIdx.x % nslab, b = blockIdx.x / nslab, h = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lo = p.offsets[b];
+    const int n = p.offsets[b + 1] - lo;
+    if (n <= 0) return;
+    if (n > nm) {
+        if (tid == 0) flag(p.status, GDN_DEV_TOO_MANY);
+        return;
+    }
+    const int hk = h / (p.hv_n / p.hk_n);
+    const Tin *qp = static_cast<const Tin *>(p.q);
+    const Tin *kp = static_cast<const Tin *>(p.k);
+    const Tin *vp = static_cast<const Tin *>(p.v);
+    Tout *op = static_cast<Tout *>(p.o);
+
+    // ---- phase 0: metadata ------------------------------------------------
+    if (tid == 0) s_maxd = 0;
+    for (int i = tid; i < nm + 2; i += kThreads) cnt[i] = 0;
+    for (int i = tid; i < n; i += kThreads) {
+        par[i] = p.parent[lo + i];
+        dep[i] = p.depth[lo + i];
+        gl[i] = p.g[(int64_t)(lo + i) * p.hv_n + h];
+        bet[i] = p.beta[(int64_t)(lo + i) * p.hv_n + h];
+    }
+    const float *s0src = p.S0 + ((int64_t)b * p.hv_n + h) * p.dv * DK + (int64_t)slab * SW * DK;
+    for (int e = tid; e < SW * DK; e += kThreads) {
+        const int c = e / DK, m = e - c * DK;
+        S0s[c * (DK + 1) + m] = s0src[e];
+    }
+    __syncthreads();
+    bool bad_tree = false, bad_desc = false;
+    for (int i = tid; i < n; i += kThreads) {
+        const int pi = par[i];
+        if (pi < -1 || pi >= i) bad_tree = true;
+        else if (dep[i] != (pi < 0 ? 1 : dep[pi] + 1)) bad_desc = true;
+    }
+    if (__syncthreads_or(bad_tree)) {
+        if (tid == 0) flag(p.status, GDN_DEV_BAD_TREE);
+        return;
+    }
+    if (__syncthreads_or(bad_desc)) {
+        if (tid == 0) flag(p.status, GDN_DEV_BAD_DESC);
+        return;
+    }
+    for (int i = tid; i < n; i += kThreads) {
+        float acc = 0.f;
+        for (int j = i; j >= 0; j = par[j]) acc += gl[j];
+        gam[i] = acc;
+        atomicAdd(&cnt[dep[i]], 1);
+        atomicMax(&s_maxd, dep[i]);
+    }
+    __syncthreads();
+    const int maxd = s_maxd;
+    if (tid == 0) {
+        int run = 0;
+        for (int d = 0; d <= maxd + 1; ++d) {
+            start[d] = run;
+            run += (d <= maxd) ? cnt[d] : 0;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < nm + 2; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+        const int d = dep[i];
+        order[start[d] + atomicAdd(&cnt[d], 1)] = i;
+    }
+
+    // ---- phase 1: S0 read-out and right-hand side -------------------------
+    float *kqw = smem + L.kq + warp * 2 * DK;
+    for (int i = warp; i < n; i += kWarps) {
+        const int64_t krow = ((int64_t)(lo + i) * p.hk_n + hk) * DK;
+        for (int m = lane; m < DK; m += 32) {
+            kqw[m] = load_f(kp, krow + m);
+            kqw[DK + m] = load_f(qp, krow + m);
+        }
+        __syncwarp();
+        if (lane < SW) {
+            float w = 0.f, z = 0.f;
+            const float *srow = S0s + lane * (DK + 1);
+#pragma unroll 8
+            for (int m = 0; m < DK; ++m) {
+                w = fmaf(srow[m], kqw[m], w);
+                z = fmaf(srow[m], kqw[DK + m], z);
+            }
+            const float vi = load_f(vp, ((int64_t)(lo + i) * p.hv_n + h) * p.dv + slab * SW + lane);
+            Ub[i * SW + lane] = bet[i] * (vi - expf(gam[i]) * w);
+            Zb[i * SW + lane] = z;
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // ---- phase 2: level-ordered forward substitution and outputs ----------
+    for (int d = 1; d <= maxd; ++d) {
+        for (int idx = start[d] + warp; idx < start[d + 1]; idx += kWarps) {
+            const int i = order[idx];
+            const int64_t krow = ((int64_t)(lo + i) * p.hk_n + hk) * DK;
+            float kr[EPL], qr[EPL];
+#pragma unroll
+            for (int r = 0; r < EPL; ++r) {
+                const int m = lane + 32 * r;
+                kr[r] = m < DK ? load_f(kp, krow + m) : 0.f;
+                qr[r] = m < DK ? load_f(qp, krow + m) : 0.f;
+            }
+            const float gi = gam[i], bi = bet[i];
+            float acc_u = lane < SW ? Ub[i * SW + lane] : 0.f;
+            float acc_o = 0.f;
+            for (int j = par[i]; j >= 0; j = par[j]) {
+                const int64_t jrow = ((int64_t)(lo + j) * p.hk_n + hk) * DK;
+                float pk = 0.f, pq = 0.f;
+#pragma unroll
+                for (int r = 0; r < EPL; ++r) {
+                    const int m = lane + 32 * r;
+                    const float kj = m < DK ? load_f(kp, jrow + m) : 0.f;
+                    pk = fmaf(kr[r], kj, pk);
+                    pq = fmaf(qr[r], kj, pq);
+                }
+                pk = warp_sum(pk);
+                pq = warp_sum(pq);
+                const float dec = expf(gi - gam[j]);
+                const float uj = lane < SW ? Ub[j * SW + lane] : 0.f;
+                acc_u -= bi * dec * pk * uj;
+                acc_o += dec * pq * uj;
+            }
+            float self = 0.f;
+#pragma unroll
+            for (int r = 0; r < EPL; ++r) self = fmaf(qr[r], kr[r], self);
+            self = warp_sum(self);
+            if (lane < SW) {
+                Ub[i * SW + lane] = acc_u;
+                const float o = p.scale * (expf(gi) * Zb[i * SW + lane] + acc_o + self * acc_u);
+                store_f(op, ((int64_t)(lo + i) * p.hv_n + h) * p.dv + slab * SW + lane, o);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename Tin, typename Tout, int DK>
+cudaError_t launch_typed(const SimtParams &p, int batch, cudaStream_t stream) {
+    const SmemLayout L = smem_layout(p.max_nodes, p.sw, DK);
+    const size_t bytes = sizeof(float) * (size_t)L.floats + sizeof(int) * (size_t)L.ints;
+    auto kern = verify_simt_kernel<Tin, Tout, DK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(p.dv / p.sw) * (unsigned)batch, p.hv_n);
+    kern<<<grid, kThreads, bytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_dk(const SimtParams &p, int dk, int batch, cudaStream_t stream) {
+    switch (dk) {
+        case 16: return launch_typed<Tin, Tout, 16>(p, batch, stream);
+        case 32: return launch_typed<Tin, Tout, 32>(p, batch, stream);
+        case 64: return launch_typed<Tin, Tout, 64>(p, batch, stream);
+        case 128: return launch_typed<Tin, Tout, 128>(p, batch, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream) {
+    SimtParams p;
+    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.dv = a.d_v; p.max_nodes = a.max_nodes;
+    p.sw = a.d_v < 32 ? a.d_v : 32;
+    p.scale = a.scale;
+    p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth;
+    p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
+    p.o = a.o; p.status = a.dev_status;
+    const bool in_bf = a.qkv_dtype == GDN_BF16, out_bf = a.out_dtype == GDN_BF16;
+    if (in_bf && out_bf) return launch_dk<__nv_bfloat16, __nv_bfloat16>(p, a.d_k, a.batch, stream);
+    if (in_bf) return launch_dk<__nv_bfloat16, float>(p, a.d_k, a.batch, stream);
+    if (out_bf) return launch_dk<float, __nv_bfloat16>(p, a.d_k, a.batch, stream);
+    return launch_dk<float, float>(p, a.d_k, a.batch, stream);
+}
+
+}  // namespace gdn

@@ -1,0 +1,178 @@
+/*
+ * gdn_tree.h -- C ABI of the GB300 (sm_103a) library for rollback-free
+ * verification of a speculative proposal tree through one Gated Delta Net layer.
+ *
+ * The operation, from "Trees from Marginals: Autoregressive drafting with
+ * factorized priors" (gist.science Technical Summary, section 3 "Rollback-Free
+ * Tree Verification for GDN"):
+ *   - a GDN layer advances its state with the gated delta rule (Challenge bullet);
+ *     this library keeps the state as S[d_v][d_k] and applies, per token t,
+ *         S_t = exp(g_t) * S_{t-1} * (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *         o_t = scale * S_t q_t
+ *     (the page writes the transpose; outputs are identical);
+ *   - a draft tree, topologically sorted, is verified in one pass: every node's
+ *     output equals the rule run along that node's root-to-node path from the
+ *     committed state S0, computed through ancestor-masked interaction matrices
+ *     and one triangular solve (Solution bullets 1-3);
+ *   - S0 is never written by verification; the state is committed in the next
+ *     iteration along the accepted branch only (Solution bullet 4).
+ *
+ * Conventions shared by every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     keeps no pointer after a call returns and allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream.
+ *   - The return value is a gdn_status.  Argument, shape, support and launch
+ *     errors are detected on the host and returned before anything is launched
+ *     (GDN_ERR_CUDA: a launch failed).  gdn_last_error() then gives a message
+ *     (thread-local, valid until the next call on the same thread).
+ *   - Data-dependent problems found on the device (a malformed tree, a bad path,
+ *     a request larger than max_nodes, a tree deeper than the bound a kernel
+ *     needs) are OR-ed into *dev_status as GDN_DEV_* bits; the kernel skips the
+ *     affected request and never traps.  The caller zeroes *dev_status before
+ *     the call and reads it after synchronising the stream.
+ *   - Requests: node_offsets[B+1] (int32, ascending, node_offsets[0] = 0)
+ *     splits the T = node_offsets[B] tree nodes into B requests; node ids in
+ *     parent[] and path_idx[] are request-local.  parent[i] = -1 marks a root
+ *     (a child of S0; forests are allowed); otherwise 0 <= parent[i] < i.
+ *   - Layouts (row-major, contiguous):
+ *       q, k   [T][Hk][d_k]      (dtype qkv_dtype)
+ *       v      [T][Hv][d_v]      (dtype qkv_dtype)
+ *       g      [T][Hv]  float32  log-decay, alpha = exp(g)
+ *       beta   [T][Hv]  float32
+ *       S0, S_new [B][Hv][d_v][d_k] float32
+ *       o      [T][Hv][d_v]      (dtype out_dtype)
+ *     Value head h reads key head h / (Hv / Hk) (Hv a multiple of Hk).
+ *   - Supported: d_k, d_v in {16, 32, 64, 128}; 1 <= max_nodes <= 256.
+ */
+#ifndef GDN_TREE_H_
+#define GDN_TREE_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent sizes */
+    GDN_ERR_UNSUPPORTED = 2,   /* a size or dtype outside the supported set */
+    GDN_ERR_INVALID_TREE = 3,  /* reserved for host-side tree checks */
+    GDN_ERR_INVALID_PATH = 4,  /* reserved for host-side path checks */
+    GDN_ERR_CUDA = 5,          /* a CUDA launch or attribute call failed */
+    GDN_ERR_DEVICE = 6         /* reserved: raised by wrappers that read dev_status */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* bits OR-ed into *dev_status */
+#define GDN_DEV_BAD_TREE      1   /* parent[i] outside [-1, i) */
+#define GDN_DEV_BAD_PATH      2   /* path not root-first or not parent->child */
+#define GDN_DEV_TOO_MANY      4   /* a request has more than max_nodes nodes */
+#define GDN_DEV_TOO_DEEP      8   /* a tree is deeper than the declared max_depth */
+#define GDN_DEV_TIMEOUT      16   /* a bounded wait inside a kernel ran out */
+#define GDN_DEV_BAD_DESC     32   /* anc_mask/depth disagree with parent[] */
+
+/*
+ * gdn_tree_build_desc -- tree descriptor ("interaction matrices representing
+ * ancestor relationships", same section, Solution bullet 2; topological order,
+ * bullet 1).
+ *   anc_mask [T][mask_words] uint32: bit j of row i (request-local ids) is set
+ *            iff node j lies on i's root-to-node path, i included.
+ *   depth    [T] int32: number of nodes on that path (a root has depth 1).
+ *   mask_words >= ceil(max_nodes / 32), at most 8.
+ * Integer work, bit-exact.  A node whose walk meets a parent outside [-1, i)
+ * gets a zero row and depth 0, and GDN_DEV_BAD_TREE is set.
+ */
+GDN_API int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offsets, int32_t batch,
+                        int32_t max_nodes, uint32_t *anc_mask, int32_t mask_words,
+                        int32_t *depth, int32_t *dev_status, void *stream);
+
+typedef struct {
+    int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
+    int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
+    int32_t max_depth;     /* caller's bound on tree depth, or 0 if unknown */
+    float scale;           /* output scale (1.0 for the plain rule) */
+    int32_t qkv_dtype;     /* gdn_dtype of q, k, v */
+    int32_t out_dtype;     /* gdn_dtype of o */
+    const int32_t *node_offsets;
+    const void *q, *k, *v;
+    const float *g, *beta, *S0;
+    const int32_t *parent;
+    const uint32_t *anc_mask;  /* from gdn_tree_build_desc */
+    int32_t mask_words;
+    const int32_t *depth;      /* from gdn_tree_build_desc */
+    void *o;
+    int32_t *dev_status;
+} gdn_verify_args;
+
+/*
+ * gdn_tree_verify -- every node's output, computed as the masked triangular
+ * solve of the same section (Solution bullets 2-3): with gamma_i the sum of g
+ * over i's path, D_ij = exp(gamma_i - gamma_j) on ancestors j of i,
+ *     X = strict-ancestor mask * beta_i * D * (K K^T)
+ *     Y = ancestor mask * D * (Q K^T)
+ *     (I + X) U = beta * (V - exp(gamma) * K S0^T)
+ *     O = scale * (exp(gamma) * Q S0^T + Y U)
+ * S0 is read, never written.  Nodes off a node's path never affect its output.
+ * Fast path: bf16 q/k/v with d_k = d_v = 128, max_nodes <= 128 and
+ * 1 <= max_depth <= 16 runs the tcgen05/TMA kernel (a deeper tree sets
+ * GDN_DEV_TOO_DEEP and its request is skipped); every other case runs the
+ * general kernel, which accepts any depth.
+ */
+GDN_API int gdn_tree_verify(const gdn_verify_args *args, void *stream);
+
+/*
+ * gdn_tree_verify_branches -- the per-branch recurrent verification the pages
+ * compare against ("Experimental Results", Verification Efficiency): one
+ * thread block per (request, value head, root-to-leaf path, d_v slab) runs the
+ * gated delta rule sequentially along its path from S0 and writes the outputs
+ * of the nodes on it.  Same arguments and results as gdn_tree_verify (up to
+ * rounding); anc_mask/depth are not read.  Used as the measurement baseline.
+ */
+GDN_API int gdn_tree_verify_branches(const gdn_verify_args *args, void *stream);
+
+typedef struct {
+    int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
+    int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
+    int32_t qkv_dtype;     /* gdn_dtype of k, v */
+    const int32_t *node_offsets;
+    const void *k, *v;
+    const float *g, *beta, *S0;
+    const int32_t *parent;
+    const int32_t *path_offsets;  /* [B+1] */
+    const int32_t *path_idx;      /* accepted path per request, request-local ids, root first */
+    float *S_new;                 /* [B][Hv][d_v][d_k]; may equal S0 (in-place commit) */
+    int32_t *dev_status;
+} gdn_commit_args;
+
+/*
+ * gdn_tree_commit -- the delayed commit (same section, Solution bullet 4): the
+ * new state after the accepted path p_1..p_L, in chunked form:
+ *     u = chain solve of the path (the verify system restricted to the path)
+ *     S_new = exp(gamma_L) S0 + sum_t exp(gamma_L - gamma_t) u_t k_t^T
+ * equal to running the rule along the path.  L = 0 leaves S0 (copied when
+ * S_new != S0).  A path that does not start at a root or does not follow
+ * parent -> child edges sets GDN_DEV_BAD_PATH and leaves that request's S_new
+ * unwritten.
+ */
+GDN_API int gdn_tree_commit(const gdn_commit_args *args, void *stream);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+GDN_API const char *gdn_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+GDN_API int gdn_tree_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_TREE_H_ */
