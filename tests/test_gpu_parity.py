@@ -286,7 +286,7 @@ def test_relabelled_tree_permutes_outputs():
 # ----------------------------------------------------------------------------
 
 def test_bad_tree_sets_status():
-    tb = W.custom(2, [np.array([-1, 0, 5, 1], np.int32)], d=16)
+    tb = W.custom(2, [np.array([-1, 0, 5, 1], np.int32)], d=16, path_fn=lambda p, r: [])
     o, status, _ = run_verify(tb)
     assert int(status.item()) & 1
 
