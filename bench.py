@@ -348,7 +348,7 @@ def dominant_kernel(tb) -> str:
     return "verify_simt"
 
 
-TC_READY = False
+TC_READY = True
 
 
 def run_reference(args, rank, world):

@@ -28,7 +28,7 @@ _I = ctypes.c_int32
 
 class VerifyArgs(ctypes.Structure):
     _fields_ = [("batch", _I), ("n_k_heads", _I), ("n_v_heads", _I), ("d_k", _I), ("d_v", _I),
-                ("max_nodes", _I), ("max_depth", _I), ("scale", ctypes.c_float),
+                ("total_nodes", _I), ("max_nodes", _I), ("max_depth", _I), ("scale", ctypes.c_float),
                 ("qkv_dtype", _I), ("out_dtype", _I), ("node_offsets", _P), ("q", _P), ("k", _P),
                 ("v", _P), ("g", _P), ("beta", _P), ("S0", _P), ("parent", _P), ("anc_mask", _P),
                 ("mask_words", _I), ("depth", _P), ("o", _P), ("dev_status", _P)]
@@ -36,7 +36,8 @@ class VerifyArgs(ctypes.Structure):
 
 class CommitArgs(ctypes.Structure):
     _fields_ = [("batch", _I), ("n_k_heads", _I), ("n_v_heads", _I), ("d_k", _I), ("d_v", _I),
-                ("max_nodes", _I), ("qkv_dtype", _I), ("node_offsets", _P), ("k", _P), ("v", _P),
+                ("total_nodes", _I), ("max_nodes", _I), ("qkv_dtype", _I), ("node_offsets", _P),
+                ("k", _P), ("v", _P),
                 ("g", _P), ("beta", _P), ("S0", _P), ("parent", _P), ("path_offsets", _P),
                 ("path_idx", _P), ("S_new", _P), ("dev_status", _P)]
 
@@ -173,7 +174,7 @@ def _verify_args(q, k, v, g, beta, S0, node_offsets, parent, anc_mask, depth, ma
     _dev(out, "out", od)
     if out.shape != (T, Hv, dv):
         raise ValueError("out must be [T, Hv, d_v]")
-    a = VerifyArgs(B, Hk, Hv, dk, dv, int(max_nodes), int(max_depth), float(scale), _code(q.dtype),
+    a = VerifyArgs(B, Hk, Hv, dk, dv, T, int(max_nodes), int(max_depth), float(scale), _code(q.dtype),
                    _code(od), _ptr(node_offsets), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                    _ptr(S0), _ptr(parent), _ptr(anc_mask), anc_mask.shape[1] if anc_mask.dim() == 2 else 1,
                    _ptr(depth), _ptr(out), _ptr(dev_status))
@@ -221,7 +222,7 @@ def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_
     if out.shape != S0.shape:
         raise ValueError("out must match S0")
     pidx = path_idx if path_idx.numel() else torch.zeros(1, dtype=torch.int32, device=k.device)
-    a = CommitArgs(B, Hk, Hv, dk, dv, int(max_nodes), _code(k.dtype), _ptr(node_offsets), _ptr(k),
+    a = CommitArgs(B, Hk, Hv, dk, dv, T, int(max_nodes), _code(k.dtype), _ptr(node_offsets), _ptr(k),
                    _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(parent), _ptr(path_offsets),
                    _ptr(pidx), _ptr(out), _ptr(dev_status))
     _check(lib().gdn_tree_commit(ctypes.byref(a), _stream(stream)))

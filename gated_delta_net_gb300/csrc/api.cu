@@ -44,6 +44,7 @@ int check_verify(const gdn_verify_args *a) {
     if (!valid_dtype(a->qkv_dtype) || !valid_dtype(a->out_dtype))
         return fail(GDN_ERR_UNSUPPORTED, "unknown dtype (qkv %d, out %d)", a->qkv_dtype, a->out_dtype);
     if (a->max_depth < 0) return fail(GDN_ERR_INVALID_ARG, "max_depth %d < 0", a->max_depth);
+    if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
     if (!std::isfinite(a->scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
     if (a->batch == 0) return GDN_OK;
     if (!a->node_offsets || !a->q || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
@@ -106,6 +107,7 @@ int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
     if (st) return st;
     if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
+    if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
     if (a->batch == 0) return GDN_OK;
     if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
         !a->path_offsets || !a->path_idx || !a->S_new)

@@ -32,7 +32,9 @@
  *     affected request and never traps.  The caller zeroes *dev_status before
  *     the call and reads it after synchronising the stream.
  *   - Requests: node_offsets[B+1] (int32, ascending, node_offsets[0] = 0)
- *     splits the T = node_offsets[B] tree nodes into B requests; node ids in
+ *     splits the T = node_offsets[B] tree nodes into B requests (the caller
+ *     also passes T as total_nodes; a request reaching past it sets
+ *     GDN_DEV_BAD_DESC and is skipped); node ids in
  *     parent[] and path_idx[] are request-local.  parent[i] = -1 marks a root
  *     (a child of S0; forests are allowed); otherwise 0 <= parent[i] < i.
  *   - Layouts (row-major, contiguous):
@@ -97,6 +99,7 @@ GDN_API int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offse
 
 typedef struct {
     int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
+    int32_t total_nodes;   /* T = node_offsets[batch]: rows of q, k, v, g, beta, o */
     int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
     int32_t max_depth;     /* caller's bound on tree depth, or 0 if unknown */
     float scale;           /* output scale (1.0 for the plain rule) */
@@ -141,6 +144,7 @@ GDN_API int gdn_tree_verify_branches(const gdn_verify_args *args, void *stream);
 
 typedef struct {
     int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
+    int32_t total_nodes;   /* T = node_offsets[batch]: rows of k, v, g, beta */
     int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
     int32_t qkv_dtype;     /* gdn_dtype of k, v */
     const int32_t *node_offsets;

