@@ -19,7 +19,7 @@ from . import build as _build
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED = 0, 1, 2
 GDN_ERR_INVALID_TREE, GDN_ERR_INVALID_PATH, GDN_ERR_CUDA, GDN_ERR_DEVICE = 3, 4, 5, 6
 GDN_F32, GDN_BF16 = 0, 1
-DEV_BITS = {1: "BAD_TREE", 2: "BAD_PATH", 4: "TOO_MANY", 8: "TOO_DEEP", 16: "TIMEOUT",
+DEV_BITS = {1: "BAD_TREE", 2: "BAD_PATH", 4: "TOO_MANY", 8: "TOO_DEEP", 16: "TIMEOUT", 64: "INTERNAL",
             32: "BAD_DESC"}
 
 _P = ctypes.c_void_p

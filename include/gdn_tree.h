@@ -81,6 +81,7 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_DEV_TOO_DEEP      8   /* a tree is deeper than the declared max_depth */
 #define GDN_DEV_TIMEOUT      16   /* a bounded wait inside a kernel ran out */
 #define GDN_DEV_BAD_DESC     32   /* anc_mask/depth disagree with parent[] */
+#define GDN_DEV_INTERNAL     64   /* a launch invariant of a kernel did not hold */
 
 /*
  * gdn_tree_build_desc -- tree descriptor ("interaction matrices representing
