@@ -227,8 +227,9 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
         gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
-                           d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes, out=S_new,
-                           dev_status=status, stream=stream)
+                           d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes,
+                           max_path=tb.max_depth_bound, out=S_new, dev_status=status,
+                           stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()

@@ -36,7 +36,8 @@ class VerifyArgs(ctypes.Structure):
 
 class CommitArgs(ctypes.Structure):
     _fields_ = [("batch", _I), ("n_k_heads", _I), ("n_v_heads", _I), ("d_k", _I), ("d_v", _I),
-                ("total_nodes", _I), ("max_nodes", _I), ("qkv_dtype", _I), ("node_offsets", _P),
+                ("total_nodes", _I), ("max_nodes", _I), ("max_path", _I), ("qkv_dtype", _I),
+                ("node_offsets", _P),
                 ("k", _P), ("v", _P),
                 ("g", _P), ("beta", _P), ("S0", _P), ("parent", _P), ("path_offsets", _P),
                 ("path_idx", _P), ("S_new", _P), ("dev_status", _P)]
@@ -202,7 +203,8 @@ def gdn_tree_verify_branches(q, k, v, g, beta, S0, node_offsets, parent, anc_mas
 
 
 def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_idx,
-                    max_nodes: int, out=None, dev_status=None, stream=None) -> torch.Tensor:
+                    max_nodes: int, max_path: int = 0, out=None, dev_status=None,
+                    stream=None) -> torch.Tensor:
     """State after each request's accepted path [B, Hv, d_v, d_k]; ``out`` may be ``S0``."""
     for name, t in (("k", k), ("v", v)):
         _dev(t, name)
@@ -222,7 +224,8 @@ def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_
     if out.shape != S0.shape:
         raise ValueError("out must match S0")
     pidx = path_idx if path_idx.numel() else torch.zeros(1, dtype=torch.int32, device=k.device)
-    a = CommitArgs(B, Hk, Hv, dk, dv, T, int(max_nodes), _code(k.dtype), _ptr(node_offsets), _ptr(k),
+    a = CommitArgs(B, Hk, Hv, dk, dv, T, int(max_nodes), int(max_path), _code(k.dtype),
+                   _ptr(node_offsets), _ptr(k),
                    _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(parent), _ptr(path_offsets),
                    _ptr(pidx), _ptr(out), _ptr(dev_status))
     _check(lib().gdn_tree_commit(ctypes.byref(a), _stream(stream)))

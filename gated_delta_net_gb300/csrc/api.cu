@@ -58,6 +58,23 @@ int check_verify(const gdn_verify_args *a) {
 
 }  // namespace
 
+namespace gdn {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace gdn
+
 extern "C" {
 
 const char *gdn_last_error(void) { return g_err; }
@@ -108,11 +125,13 @@ int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     if (st) return st;
     if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
     if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
+    if (a->max_path < 0) return fail(GDN_ERR_INVALID_ARG, "max_path %d < 0", a->max_path);
     if (a->batch == 0) return GDN_OK;
     if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
         !a->path_offsets || !a->path_idx || !a->S_new)
         return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
-    cudaError_t e = gdn::launch_commit_simt(*a, (cudaStream_t)stream);
+    cudaError_t e = gdn::commit_fast_supported(*a) ? gdn::launch_commit_fast(*a, (cudaStream_t)stream)
+                                                   : gdn::launch_commit_simt(*a, (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
 }
 

@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "gdn_tree.h"
@@ -41,6 +42,13 @@ cudaError_t launch_build_desc(const int32_t *parent, const int32_t *node_offsets
 cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream);
 cudaError_t launch_verify_branches(const gdn_verify_args &a, cudaStream_t stream);
 cudaError_t launch_commit_simt(const gdn_commit_args &a, cudaStream_t stream);
+
+// TMA-staged commit for d_k = d_v = 128 and accepted paths of at most 16 nodes
+bool commit_fast_supported(const gdn_commit_args &a);
+cudaError_t launch_commit_fast(const gdn_commit_args &a, cudaStream_t stream);
+
+// driver entry point for TMA descriptors (nullptr when the driver lacks it)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // tcgen05/TMA fast path; returns cudaErrorNotSupported when the shape is not covered
 bool verify_tc_supported(const gdn_verify_args &a);

@@ -30,8 +30,6 @@
 // zero in the output product and its subtree's outputs set to NaN, so
 // non-finite values never leave their own branch.
 #include <cuda_fp16.h>
-#include <cudaTypedefs.h>
-
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -517,23 +515,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void *ptr = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
 // [T][H][128] bf16 viewed as a 3-D tensor (d, head, token); boxes of 64 x 1 x 32,
 // 128-byte swizzle.
 bool encode_tokens(CUtensorMap *map, const void *base, int heads, int total) {
-    auto enc = get_encoder();
+    auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)total};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
@@ -551,7 +536,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 bool verify_tc_supported(const gdn_verify_args &a) {
     return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && a.max_nodes <= kN &&
            a.max_depth >= 1 && a.max_depth <= kMaxDepth && a.total_nodes > 0 && aligned16(a.q) &&
-           aligned16(a.k) && aligned16(a.v) && aligned16(a.S0) && aligned16(a.o) && get_encoder() != nullptr;
+           aligned16(a.k) && aligned16(a.v) && aligned16(a.S0) && aligned16(a.o) && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream) {

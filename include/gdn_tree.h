@@ -147,6 +147,7 @@ typedef struct {
     int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
     int32_t total_nodes;   /* T = node_offsets[batch]: rows of k, v, g, beta */
     int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
+    int32_t max_path;      /* caller's bound on accepted-path length, or 0 if unknown */
     int32_t qkv_dtype;     /* gdn_dtype of k, v */
     const int32_t *node_offsets;
     const void *k, *v;
@@ -166,7 +167,11 @@ typedef struct {
  * equal to running the rule along the path.  L = 0 leaves S0 (copied when
  * S_new != S0).  A path that does not start at a root or does not follow
  * parent -> child edges sets GDN_DEV_BAD_PATH and leaves that request's S_new
- * unwritten.
+ * unwritten.  Everything accumulates in fp32.
+ * Fast path: d_k = d_v = 128 and 1 <= max_path <= 16 runs one thread block per
+ * (request, value head) with the state tile moved by TMA (a longer path sets
+ * GDN_DEV_TOO_DEEP and its request is skipped); every other case runs the
+ * general kernel.
  */
 GDN_API int gdn_tree_commit(const gdn_commit_args *args, void *stream);
 

@@ -77,13 +77,14 @@ def test_verify_empty_batch_is_a_no_op(L):
 def test_commit_rejects_bad_arguments(L):
     fake = ctypes.c_void_p(0x1000)
     base = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, total_nodes=12, max_nodes=12,
-                qkv_dtype=0,
+                max_path=0, qkv_dtype=0,
                 node_offsets=fake, k=fake, v=fake, g=fake, beta=fake, S0=fake, parent=fake,
                 path_offsets=fake, path_idx=fake, S_new=fake, dev_status=fake)
     for kw, code in ((dict(S_new=None), binding.GDN_ERR_INVALID_ARG),
                      (dict(d_k=8), binding.GDN_ERR_UNSUPPORTED),
                      (dict(max_nodes=300), binding.GDN_ERR_UNSUPPORTED),
-                     (dict(qkv_dtype=3), binding.GDN_ERR_UNSUPPORTED)):
+                     (dict(qkv_dtype=3), binding.GDN_ERR_UNSUPPORTED),
+                     (dict(max_path=-1), binding.GDN_ERR_INVALID_ARG)):
         a = binding.CommitArgs(**{**base, **kw})
         assert L.gdn_tree_commit(ctypes.byref(a), None) == code
     assert L.gdn_tree_commit(None, None) == binding.GDN_ERR_INVALID_ARG
