@@ -107,6 +107,22 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def reduce_max(x: float, device=None) -> float:
+    """Maximum of x over the ranks of the default process group (x if there is none)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, steps: int, seconds: float, world: int) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world * steps / seconds
+
+
 # ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
@@ -259,13 +275,8 @@ def run_ours(args, rank, world, local_rank):
     gb.check_status(status)
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     verify_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    nodes = T * world
-    value = nodes * args.steps / total_s
+    total_s = reduce_max(sum(step_ms) / 1e3, dev)
+    value = job_throughput(T, args.steps, total_s, world)
     ms_per_step = total_s * 1e3 / args.steps
 
     # end to end through the public API: pinned host inputs in, o and S_new out
@@ -290,12 +301,8 @@ def run_ours(args, rank, world, local_rank):
         if it > 0:
             e2e_ev.append((e0, e1))
     torch.cuda.synchronize()
-    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = nodes * e2e_steps / e2e_s
+    e2e_s = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, dev)
+    e2e_value = job_throughput(T, e2e_steps, e2e_s, world)
 
     if rank != 0:
         return None

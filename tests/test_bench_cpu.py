@@ -1,0 +1,77 @@
+"""CPU checks of the benchmark's host logic: the cross-rank reduction (two gloo
+ranks), the byte and FLOP accounting, and the oracle reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from gated_delta_net_gb300 import workloads as W  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    elapsed = [0.5, 2.0][rank]
+    t = bench.reduce_max(elapsed)
+    q.put((rank, t, bench.job_throughput(1000, 10, t, world)))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_reduction_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, t, v in out:
+        assert t == 2.0
+        assert v == pytest.approx(1000 * 2 * 10 / 2.0)
+
+
+def test_reduce_max_without_process_group():
+    assert bench.reduce_max(3.5) == 3.5
+
+
+def test_verify_bytes_throughput_point():
+    tb = W.serving_target()
+    # per request: S0 + 128 nodes x (q,k + v + g,beta + o + parent + depth + 4 mask words)
+    per_req = 32 * 128 * 128 * 4 + 128 * (2 * 16 * 128 * 2 + 32 * 128 * 2 + 32 * 8 + 32 * 128 * 2 + 4 + 4 + 16)
+    assert bench.verify_bytes(tb) == 64 * per_req + 4 * 65
+
+
+def test_verify_flops_chain_closed_form():
+    tb = W.custom(1, [W.chain_tree(10)], n_k_heads=1, n_v_heads=1, d=16)
+    P = sum(range(1, 11))
+    assert bench.verify_flops(tb) == 4 * 10 * 16 * 16 + 2 * 16 * (4 * P - 2 * 10)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--batch", "2", "--tree-size", "16",
+                        "--ref-seconds", "0.05"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["unit"] == bench.UNIT and line["higher_is_better"] is True
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
