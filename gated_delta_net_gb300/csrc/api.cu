@@ -130,8 +130,9 @@ int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
         !a->path_offsets || !a->path_idx || !a->S_new)
         return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
-    cudaError_t e = gdn::commit_fast_supported(*a) ? gdn::launch_commit_fast(*a, (cudaStream_t)stream)
-                                                   : gdn::launch_commit_simt(*a, (cudaStream_t)stream);
+    cudaError_t e = gdn::commit_tc_supported(*a)     ? gdn::launch_commit_tc(*a, (cudaStream_t)stream)
+                    : gdn::commit_fast_supported(*a) ? gdn::launch_commit_fast(*a, (cudaStream_t)stream)
+                                                     : gdn::launch_commit_simt(*a, (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
 }
 

@@ -47,6 +47,10 @@ cudaError_t launch_commit_simt(const gdn_commit_args &a, cudaStream_t stream);
 bool commit_fast_supported(const gdn_commit_args &a);
 cudaError_t launch_commit_fast(const gdn_commit_args &a, cudaStream_t stream);
 
+// tensor-core commit for bf16 k/v, d_k = d_v = 128 and paths of at most 16 nodes
+bool commit_tc_supported(const gdn_commit_args &a);
+cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream);
+
 // driver entry point for TMA descriptors (nullptr when the driver lacks it)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
