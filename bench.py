@@ -41,6 +41,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
     "verify_simt": ["gated_delta_net_gb300/csrc/verify_simt.cu"],
+    "commit_tc": ["gated_delta_net_gb300/csrc/commit_tc.cu"],
 }
 
 
@@ -128,7 +129,7 @@ def job_throughput(units_per_rank: int, steps: int, seconds: float, world: int) 
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -144,7 +145,13 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            time.sleep(0.5)          # let the sampler start before the timed region
         return self
+
+    def mark(self, which: str):
+        """Record the wall-clock start or end of the timed region."""
+        setattr(self, which, time.time())
 
     def __exit__(self, *exc):
         self.lines = []
@@ -157,32 +164,44 @@ class ClockSampler:
     def summary(self):
         if not getattr(self, "lines", None):
             return None
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            try:
-                sm.append(float(parts[0]))
-                mx = max(mx, float(parts[1]))
-            except (ValueError, IndexError):
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.lines, getattr(self, "start", None), getattr(self, "end", None))
+
+
+def summarize_clocks(lines, start=None, end=None):
+    """Median SM clock and throttle reasons of the nvidia-smi samples taken
+    inside [start, end] (wall-clock seconds); all samples if none fall inside."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, mx = float(parts[1]), float(parts[2])
+        except (ValueError, IndexError):
+            continue
+        rows.append((ts, sm, mx, {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
+    if not rows:
+        return None
+    inside = [r for r in rows if start is not None and end is not None and start <= r[0] <= end]
+    use = inside or rows
+    reasons = set().union(*(r[3] for r in use))
+    return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+            "reasons": sorted(reasons), "samples": len(use),
+            "window": "timed region" if inside else "around the timed region"}
 
 
 # ----------------------------------------------------------------------------
 # the CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(tb, seconds: float, seed: int = 0):
+def oracle_sample(tb, seconds: float, seed: int = 0, prepared=None):
     """Time the float64 oracle on a random sample of (request, value head, node)
-    outputs sized to take about `seconds`; returns (node-tokens/s, threads, desc)."""
+    outputs sized to take about `seconds`; returns (node-tokens/s, threads, desc).
+    The one-time conversion of the inputs to float64 (`prepared`) is not timed."""
     import oracle
+    if prepared is None:
+        prepared = oracle.prepare(tb)
     rng = np.random.default_rng(seed)
     threads = oracle.default_threads()
     sizes = tb.sizes()
@@ -194,12 +213,12 @@ def oracle_sample(tb, seconds: float, seed: int = 0):
 
     m = 4 * threads
     t0 = time.perf_counter()
-    oracle.verify_selected(tb, draw(m), threads)
+    oracle.verify_selected(tb, draw(m), threads, prepared)
     dt = time.perf_counter() - t0
     m = int(min(max(m * seconds / max(dt, 1e-3), m), 2_000_000))
     sel = draw(m)
     t0 = time.perf_counter()
-    oracle.verify_selected(tb, sel, threads)
+    oracle.verify_selected(tb, sel, threads, prepared)
     dt = time.perf_counter() - t0
     value = (m / tb.n_v_heads) / dt
     desc = (f"{m} random (request, value head, node) outputs of the workload, each a "
@@ -264,12 +283,14 @@ def run_ours(args, rank, world, local_rank):
     except Exception:
         gpu_id = str(local_rank)
     with ClockSampler(gpu_id) as clk:
+        clk.mark("start")
         for e in evs:
             flush.zero_()
             e[0].record(stream)
             step((e[2], e[3]))
             e[1].record(stream)
         torch.cuda.synchronize()
+        clk.mark("end")
     if world > 1:
         torch.distributed.barrier()
     gb.check_status(status)
@@ -367,8 +388,11 @@ def run_reference(args, rank, world):
     vals, ts = [], []
     import oracle
     oracle.build()
+    # each step is a bounded sample; the whole run stays within --ref-budget seconds
+    per_step = min(args.ref_seconds, args.ref_budget / (args.warmup + args.steps))
+    prepared = oracle.prepare(tb)
     for i in range(args.warmup + args.steps):
-        v, threads, desc, dt = oracle_sample(tb, args.ref_seconds, seed=i)
+        v, threads, desc, dt = oracle_sample(tb, per_step, seed=i, prepared=prepared)
         if i >= args.warmup:
             vals.append(v)
             ts.append(dt)
@@ -390,13 +414,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--tree-size", type=int, default=128)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -295,7 +295,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
         } else {
             for (int q = 0; q < 4; ++q) tma_store_2d(&tmSN, tile + q * kD * 32, q * 32, tile_row);
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read();
         }
         if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
     }

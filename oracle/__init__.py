@@ -116,12 +116,19 @@ def verify(tb, nthreads: Optional[int] = None) -> np.ndarray:
     return o
 
 
-def verify_selected(tb, sel, nthreads: Optional[int] = None) -> np.ndarray:
-    """Outputs [len(sel), d_v] of the selected (request, value head, local node) triples."""
+def prepare(tb):
+    """The workload's arrays in the oracle's own layout (int32 / float64 copies),
+    so that repeated calls on one workload convert them once."""
+    return [_i32(tb.node_offsets), _i32(tb.parent), _f64(tb.q), _f64(tb.k), _f64(tb.v),
+            _f64(tb.g), _f64(tb.beta), _f64(tb.S0)]
+
+
+def verify_selected(tb, sel, nthreads: Optional[int] = None, prepared=None) -> np.ndarray:
+    """Outputs [len(sel), d_v] of the selected (request, value head, local node) triples.
+    `prepared` is the result of prepare(tb), when the caller holds one."""
     sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int64).reshape(-1, 3))
     o = np.zeros((len(sel), tb.d_v), np.float64)
-    keep = [_i32(tb.node_offsets), _i32(tb.parent), _f64(tb.q), _f64(tb.k), _f64(tb.v),
-            _f64(tb.g), _f64(tb.beta), _f64(tb.S0)]
+    keep = prepared if prepared is not None else prepare(tb)
     st = _load().gdn_oracle_verify_sel(*_dims(tb), *[_p(a) for a in keep], float(tb.scale),
                                        _p(sel), len(sel), _p(o), nthreads or default_threads())
     if st:

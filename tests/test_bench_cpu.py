@@ -75,3 +75,22 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["unit"] == bench.UNIT and line["higher_is_better"] is True
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_summary_keeps_only_the_timed_window():
+    import datetime
+    import bench
+
+    def line(sec, mhz, thermal="Not Active"):
+        t = datetime.datetime(2026, 1, 1, 12, 0, sec, 500000).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{t}, {mhz}, 2070, 900.1, 0x0, Not Active, {thermal}, Not Active, Not Active"
+
+    lines = [line(0, 1000), line(1, 2070), line(2, 2000, "Active"), line(3, 2070), line(9, 500)]
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 1).timestamp()
+    s = bench.summarize_clocks(lines, t0, t0 + 3)
+    assert s["window"] == "timed region" and s["samples"] == 3
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["hw_thermal_slowdown"]
+    s = bench.summarize_clocks(lines, t0 + 100, t0 + 101)
+    assert s["window"] == "around the timed region" and s["samples"] == 5
+    assert bench.summarize_clocks([]) is None
