@@ -261,7 +261,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             if (!__any_sync(0xffffffffu, dm != 0u)) continue;
             uint32_t v[32];
             tmem_ld32_nowait(tmem + lane_base + col0 + cc * 32, v);
-            tmem_wait_ld();
+            tmem_wait_ld_into(v);
 #pragma unroll
             for (int c = 0; c < 32; ++c)
                 if ((dm >> c) & 1u) dst[(cc * 32 + c) * kMaxDepth + da - 1] = __float2half_rn(__uint_as_float(v[c]));
@@ -272,9 +272,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         // ===================== tree warps ======================================
         const int i = tid;
         const int myd = i < n ? dep[i] : 0;
-        if (i == 0) {
-            // Gram: K [K;Q]^T -> columns [0, 256), as soon as the tiles land
-            ok = mbar_wait(&bar[B_KQ], 0) && ok;
+        // Gram: K [K;Q]^T -> columns [0, 256), issued by thread 0 once the tiles
+        // have landed: now if they have, else after the descendant rows
+        bool gram_issued = false;
+        auto issue_gram = [&]() {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -282,7 +283,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 mma_bf16(tmem, d, d, id_n256, ks > 0);
             }
             mma_commit(&bar[B_GRAM]);
-        }
+            gram_issued = true;
+        };
+        if (i == 0 && mbar_test(&bar[B_KQ], 0)) issue_gram();
         // paths (the set bits of each mask row, root first) and gamma
         if (i < n) {
             float acc = 0.f;
@@ -305,18 +308,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             egt[i] = 0.f;
             eg[i] = 1.f;
         }
-        named_sync(1, 128);
-        // mask rows become descendant rows: bit i of row a iff a is on i's path
+        // mask rows become descendant rows: bit i of row a iff a is on i's path.
+        // Tree warp w owns word w of every row: the transpose of the 32 x 32 bit
+        // block (its nodes i) x (word c of their ancestor rows), by five rounds of
+        // shuffles (block transpose of Hacker's Delight, section 7-3, on
+        // bit-reversed words so that bit c stands for column c); zero for c > w.
+        {
+            uint32_t anc[4], mine[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) msk[i * 4 + w] = 0u;
-        named_sync(1, 128);
+            for (int c = 0; c < 4; ++c) {
+                anc[c] = msk[i * 4 + c];
+                mine[c] = 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c > quad) break;  // warp-uniform
+                uint32_t x = __brev(anc[c]);
+                uint32_t m = 0x0000FFFFu;
+#pragma unroll
+                for (int j = 16; j != 0; j >>= 1, m ^= (m << j)) {
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, x, j);
+                    x = (lane & j) ? x ^ (((other ^ (x >> j)) & m) << j) : x ^ ((x ^ (other >> j)) & m);
+                }
+                mine[c] = __brev(x);
+            }
+            named_sync(1, 128);  // every ancestor row has been read
+#pragma unroll
+            for (int c = 0; c < 4; ++c) msk[(c * 32 + lane) * 4 + quad] = mine[c];
+        }
         const uint4 pr = *reinterpret_cast<const uint4 *>(path + i * kMaxDepth);
         const uint32_t pw[4] = {pr.x, pr.y, pr.z, pr.w};
         int node_at[kMaxDepth];
 #pragma unroll
-        for (int l = 0; l < kMaxDepth; ++l) {
-            node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0xFFu) : i;
-            if (l < myd) atomicOr(&msk[node_at[l] * 4 + (i >> 5)], 1u << (i & 31));
+        for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0xFFu) : i;
+        if (i == 0 && !gram_issued) {
+            ok = mbar_wait(&bar[B_KQ], 0) && ok;
+            issue_gram();
         }
         named_sync(1, 128);
         mbar_arrive(&bar[B_DESC]);
@@ -421,16 +448,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                     tma_load_3d(sm + OFF_S0 + h * 16384 + r * 4096, &tmV, &bar[B_V], h * 64, hv, lo + 32 * r);
         }
 
-        // right-hand side rows R[j][n] = beta_j (v[j][n] - e^gamma_j W[j][n]) (MN-major B)
+        // right-hand side rows R[j][n] = beta_j v[j][n] - beta_j e^gamma_j W[j][n] (MN-major B).
+        // A row with a non-finite entry is stored as zero (its subtree's outputs are
+        // set to NaN), and so is every row past the tree.
         const int j = row;
         ok = mbar_wait(&bar[B_V], 0) && ok;
         tc_fence_after();
-        const float bj = bet[j], ej = egt[j];
-        bool bad = false;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            float w[32];
-            tmem_ld32(tmem + lane_base + cc * 32, w);
+        const float bj = bet[j], bej = bj * egt[j];
+        float chk = 0.f;  // 0 * x: stays zero while every entry is finite
+        auto r_chunk = [&](const uint32_t (&w)[32], int cc) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int n0 = cc * 32 + q * 8;
@@ -440,14 +466,34 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float vj = (e & 1) ? bf16_hi(vw[e >> 1]) : bf16_lo(vw[e >> 1]);
-                    float x = bj * (vj - ej * w[q * 8 + e]);
-                    const bool fin = isfinite(x);
-                    bad |= !fin;
-                    r[e] = (fin && j < n) ? x : 0.f;
+                    r[e] = fmaf(-bej, __uint_as_float(w[q * 8 + e]), bj * vj);
+                    chk = fmaf(0.f, r[e], chk);
                 }
                 *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, n0)) =
                     make_uint4(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]), pack_bf16(r[4], r[5]), pack_bf16(r[6], r[7]));
             }
+        };
+        {
+            // W columns 32 at a time, the next load in flight while one is used
+            uint32_t wa[32], wb[32];
+            tmem_ld32_nowait(tmem + lane_base, wa);
+            tmem_wait_ld_into(wa);
+            tmem_ld32_nowait(tmem + lane_base + 32, wb);
+            r_chunk(wa, 0);
+            tmem_wait_ld_into(wb);
+            tmem_ld32_nowait(tmem + lane_base + 64, wa);
+            r_chunk(wb, 1);
+            tmem_wait_ld_into(wa);
+            tmem_ld32_nowait(tmem + lane_base + 96, wb);
+            r_chunk(wa, 2);
+            tmem_wait_ld_into(wb);
+            r_chunk(wb, 3);
+        }
+        const bool bad = chk != 0.f;
+        if (bad || j >= n) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, q * 8)) = make_uint4(0u, 0u, 0u, 0u);
         }
         if (bad && j < n) {  // the row and every node below it
 #pragma unroll
@@ -480,15 +526,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         tc_fence_after();
         const int i = row;
         const bool hit = (pset[i >> 5] >> (i & 31)) & 1u;
-        const float f = p.scale * eg[i];
+        const float f = hit ? __int_as_float(0x7fc00000) : p.scale * eg[i];  // NaN * z is NaN
         constexpr int kRowBytes = kD * (int)sizeof(Tout);
         uint8_t *srow = sm + OFF_KQ + i * (kRowBytes + 16);
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        auto o_chunk = [&](const uint32_t (&zr)[32], int cc) {
             float z[32];
-            tmem_ld32(tmem + lane_base + 128 + cc * 32, z);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) z[e] = hit ? __int_as_float(0x7fc00000) : f * z[e];
+            for (int e = 0; e < 32; ++e) z[e] = f * __uint_as_float(zr[e]);
             if constexpr (sizeof(Tout) == 2) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -501,6 +545,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                     *reinterpret_cast<float4 *>(srow + (cc * 8 + q) * 16) =
                         make_float4(z[q * 4 + 0], z[q * 4 + 1], z[q * 4 + 2], z[q * 4 + 3]);
             }
+        };
+        {
+            uint32_t za[32], zb[32];
+            tmem_ld32_nowait(tmem + lane_base + 128, za);
+            tmem_wait_ld_into(za);
+            tmem_ld32_nowait(tmem + lane_base + 160, zb);
+            o_chunk(za, 0);
+            tmem_wait_ld_into(zb);
+            tmem_ld32_nowait(tmem + lane_base + 192, za);
+            o_chunk(zb, 1);
+            tmem_wait_ld_into(za);
+            tmem_ld32_nowait(tmem + lane_base + 224, zb);
+            o_chunk(za, 2);
+            tmem_wait_ld_into(zb);
+            o_chunk(zb, 3);
         }
         if (i < n) {
             fence_proxy_async_smem();
