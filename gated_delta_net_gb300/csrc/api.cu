@@ -73,6 +73,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+int sm_count() {
+    static int count = 0;
+    if (!count) {
+        int dev = 0, c = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1)
+            return 1;
+        count = c;
+    }
+    return count;
+}
+
 }  // namespace gdn
 
 extern "C" {

@@ -54,6 +54,9 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream);
 // driver entry point for TMA descriptors (nullptr when the driver lacks it)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// streaming multiprocessors on the current device (1 if the query fails)
+int sm_count();
+
 // tcgen05/TMA fast path; returns cudaErrorNotSupported when the shape is not covered
 bool verify_tc_supported(const gdn_verify_args &a);
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream);

@@ -25,11 +25,17 @@
 //   warps 0-3 ("tree"):  node metadata, paths, gamma; scatter of the Gram into
 //                        per-node ancestor rows; X scaling; P; P rows.
 //   warps 4-7 ("state"): S0 conversion; right-hand side R rows; epilogue.
-//   thread 128 also issues the TMA copies and every MMA.
+//   thread 128 issues the TMA copies and the S0 and output MMAs, thread 0 the Gram.
+// The grid is persistent (two blocks per SM); a block walks its (request, value
+// head) items and overlaps the next item's tree metadata, K/Q tiles and S0
+// conversion with the current item's right-hand side, output MMA and epilogue.
+// Every mbarrier completes once per item, so waits use the item's parity.
 // A node whose right-hand side row turns non-finite has that row replaced by
 // zero in the output product and its subtree's outputs set to NaN, so
 // non-finite values never leave their own branch.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -55,24 +61,60 @@ constexpr int OFF_MASK = OFF_Y + kN * kMaxDepth * 2;    // uint32 [128][4] ances
 constexpr int OFF_PATH = OFF_MASK + kN * 4 * 4;         // uint8 [128][16]
 constexpr int OFF_F = OFF_PATH + kN * kMaxDepth;        // float graw, gam, egt, eg, bet [128]
 constexpr int OFF_I = OFF_F + 5 * kN * 4;               // int dep, par [128]
-constexpr int OFF_MISC = OFF_I + 2 * kN * 4;            // tmem slot, poisoned-node set[4], err
+constexpr int OFF_MISC = OFF_I + 2 * kN * 4;            // tmem slot, poisoned-node sets[2][4], errors[2]
 constexpr int OFF_BAR = OFF_MISC + 64;
-constexpr int kBars = 11;
+constexpr int kBars = 12;
 constexpr int kSmemBytes = OFF_BAR + kBars * 8;
 
 // mbarrier indices
-enum { B_KQ, B_GRAM, B_DESC, B_TFREE, B_S0IN, B_S0, B_R, B_P, B_OUT, B_V, B_SPARE };
+enum { B_KQ, B_GRAM, B_DESC, B_TFREE, B_S0IN, B_S0, B_R, B_P, B_OUT, B_V, B_META, B_ZFREE };
 
 struct TcParams {
-    int hk_n, hv_n, words, total;
+    int hk_n, hv_n, words, total, items;
     float scale;
     const int32_t *offsets, *parent, *depth;
     const uint32_t *mask;
-    const __nv_bfloat16 *v;
     const float *g, *beta, *S0;
     void *o;
     int32_t *status;
 };
+
+// one (request, value head) work item
+struct Item {
+    int idx, b, hv, hk, lo, n;
+};
+
+__device__ __forceinline__ bool item_ok(int lo, int n, int total) {
+    return n > 0 && n <= kN && lo >= 0 && lo + n <= total;
+}
+
+__device__ __forceinline__ void set_item(const TcParams &p, int idx, int lo, int n, Item &it) {
+    it.idx = idx;
+    it.b = idx / p.hv_n;
+    it.hv = idx % p.hv_n;
+    it.hk = it.hv / (p.hv_n / p.hk_n);
+    it.lo = lo;
+    it.n = n;
+}
+
+// The first item at or after idx (stride `step`) whose request is non-empty and
+// well placed; requests that are too large or reach past the node count are
+// flagged (when `report`) and passed over.
+__device__ bool find_item(const TcParams &p, int idx, int step, bool report, Item &it) {
+    for (; idx < p.items; idx += step) {
+        const int b = idx / p.hv_n;
+        const int lo = __ldg(p.offsets + b);
+        const int n = __ldg(p.offsets + b + 1) - lo;
+        if (n == 0) continue;
+        if (!item_ok(lo, n, p.total)) {
+            if (report) flag(p.status, n > kN ? GDN_DEV_TOO_MANY : GDN_DEV_BAD_DESC);
+            continue;
+        }
+        set_item(p, idx, lo, n, it);
+        return true;
+    }
+    return false;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -109,7 +151,7 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 template <typename Tout>
 __global__ void __launch_bounds__(kT, 2)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                 const __grid_constant__ CUtensorMap tmV, TcParams p) {
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, TcParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __half *Xs = reinterpret_cast<__half *>(sm + OFF_X);
     __half *Ys = reinterpret_cast<__half *>(sm + OFF_Y);
@@ -119,37 +161,30 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     float *gam = graw + kN, *egt = graw + 2 * kN, *eg = graw + 3 * kN, *bet = graw + 4 * kN;
     int *dep = reinterpret_cast<int *>(sm + OFF_I), *par = dep + kN;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
-    uint32_t *pset = tslot + 1;  // nodes whose output is poisoned
-    int *s_err = reinterpret_cast<int *>(tslot + 5);
+    uint32_t *pset = tslot + 1;                           // [parity][4]: nodes whose output is poisoned
+    int *s_err = reinterpret_cast<int *>(tslot + 9);      // [parity]: descriptor errors of the item
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
     const bool tree = warp < 4;
-    const int hv = blockIdx.x % p.hv_n, b = blockIdx.x / p.hv_n;
-    const int hk = hv / (p.hv_n / p.hk_n);
-    const int lo = p.offsets[b];
-    const int n = p.offsets[b + 1] - lo;
-    if (n <= 0) return;
-    if (n > kN || lo < 0 || lo + n > p.total || (smem_u32(sm) & 1023u) != 0u) {
-        if (tid == 0)
-            flag(p.status, n > kN ? GDN_DEV_TOO_MANY : ((smem_u32(sm) & 1023u) ? GDN_DEV_INTERNAL : GDN_DEV_BAD_DESC));
-        return;
-    }
     const int row = quad * 32 + lane;  // tensor-memory lane of this thread = a tree node
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const bool issuer = tid == 128;
-    const int nbox = (n + 31) >> 5;
+    if ((smem_u32(sm) & 1023u) != 0u) {
+        if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
+        return;
+    }
+    Item cur;
+    if (!find_item(p, blockIdx.x, gridDim.x, tid == 0, cur)) return;
 
-    // ---- set-up -------------------------------------------------------------
+    // ---- set-up, once per block ---------------------------------------------
     if (tid == 0) {
         for (int k = 0; k < kBars; ++k) {
-            const uint32_t count = k == B_TFREE ? 256 : (k == B_DESC || k == B_S0IN || k == B_R || k == B_P) ? 128 : 1;
-            mbar_init(&bar[k], count);
+            const bool one = k == B_KQ || k == B_GRAM || k == B_S0 || k == B_OUT || k == B_V;
+            mbar_init(&bar[k], k == B_TFREE ? 256u : one ? 1u : 128u);
         }
         fence_mbar_init();
-        *s_err = 0;
     }
-    if (tid < 4) pset[tid] = 0u;
     if (warp == 0) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
@@ -160,140 +195,76 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const uint32_t tmem = *tslot;
     bool ok = true;
 
-    // state warps convert S0 rows 32 sw .. 32 sw + 31, eight rows per batch,
-    // double-buffered; lane l holds columns 4l .. 4l + 3 (coalesced row reads)
-    const int sw = warp - 4;
-    const float *s0t = p.S0 + ((int64_t)b * p.hv_n + hv) * (kD * kD);
-    float4 s0a[8], s0b[8];
-    auto s0_load = [&](float4 (&dst)[8], int batch) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-            dst[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (sw * 32 + batch * 8 + r) * kD) + lane);
-    };
-    auto s0_put = [&](const float4 (&src)[8], int batch) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-            *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(sw * 32 + batch * 8 + r, 4 * lane)) =
-                make_uint2(pack_bf16(src[r].x, src[r].y), pack_bf16(src[r].z, src[r].w));
+    // K and Q tiles of an item (boxes of 32 nodes x 64 features, both k-blocks)
+    auto issue_kq = [&](const Item &it) {
+        const int nb = (it.n + 31) >> 5;
+        mbar_arrive_expect_tx(&bar[B_KQ], (uint32_t)(2 * 2 * nb * 4096));
+        for (int kb = 0; kb < 2; ++kb)
+            for (int r = 0; r < nb; ++r) {
+                tma_load_3d(sm + OFF_KQ + kb * 32768 + r * 4096, &tmK, &bar[B_KQ], kb * 64, it.hk, it.lo + 32 * r);
+                tma_load_3d(sm + OFF_KQ + kb * 32768 + (128 + 32 * r) * 128, &tmQ, &bar[B_KQ], kb * 64, it.hk,
+                            it.lo + 32 * r);
+            }
     };
 
-    if (tree) {
-        // ---- node metadata (thread i = node i) -------------------------------
+    // Tree warps: an item's node metadata, validation, paths, gamma and
+    // descendant rows into shared memory, then arrive on B_DESC.
+    auto tree_meta = [&](const Item &it, int pp) {
         const int i = tid;
-        if (i < n) {
-            par[i] = p.parent[lo + i];
-            dep[i] = p.depth[lo + i];
+        int pi = -1, di = 0;
+        uint32_t mw[4] = {0u, 0u, 0u, 0u};
+        float gr = 0.f, br = 0.f;
+        if (i < it.n) {
+            const int64_t gi = it.lo + i;
+            pi = __ldg(p.parent + gi);
+            di = __ldg(p.depth + gi);
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                msk[i * 4 + w] = w < p.words ? p.mask[(int64_t)(lo + i) * p.words + w] : 0u;
-            graw[i] = p.g[(int64_t)(lo + i) * p.hv_n + hv];
-            bet[i] = p.beta[(int64_t)(lo + i) * p.hv_n + hv];
-        } else {
-            par[i] = -1;
-            dep[i] = 0;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) msk[i * 4 + w] = 0u;
-            graw[i] = 0.f;
-            bet[i] = 0.f;
+            for (int w = 0; w < 4; ++w) mw[w] = w < p.words ? __ldg(p.mask + gi * p.words + w) : 0u;
+            gr = __ldg(p.g + gi * p.hv_n + it.hv);
+            br = __ldg(p.beta + gi * p.hv_n + it.hv);
         }
+        named_sync(1, 128);  // the previous item's tree data is no longer read
+        par[i] = pi;
+        dep[i] = di;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) msk[i * 4 + w] = mw[w];
+        graw[i] = gr;
+        bet[i] = br;
         // raw ancestor rows start at zero (entries past a node's depth stay zero)
         reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        if (issuer) {
-            mbar_arrive_expect_tx(&bar[B_KQ], (uint32_t)(2 * 2 * nbox * 4096));
-            for (int kb = 0; kb < 2; ++kb)
-                for (int r = 0; r < nbox; ++r) {
-                    tma_load_3d(sm + OFF_KQ + kb * 32768 + r * 4096, &tmK, &bar[B_KQ], kb * 64, hk, lo + 32 * r);
-                    tma_load_3d(sm + OFF_KQ + kb * 32768 + (128 + 32 * r) * 128, &tmQ, &bar[B_KQ], kb * 64, hk,
-                                lo + 32 * r);
-                }
-        }
-        s0_load(s0a, 0);
-        s0_load(s0b, 1);
-    }
-    __syncthreads();
-
-    if (tree) {
-        // ---- validation --------------------------------------------------------
-        const int i = tid, pi = par[i];
-        if (i < n) {
+        if (i < 4) pset[pp * 4 + i] = 0u;
+        if (i == 0) s_err[pp] = 0;
+        named_sync(1, 128);
+        // validation: parent in [-1, i), depth and mask row consistent with the parent's
+        if (i < it.n) {
             int e = 0;
             if (pi < -1 || pi >= i) {
                 e = GDN_DEV_BAD_TREE;
             } else {
                 const int want = pi < 0 ? 1 : dep[pi] + 1;
-                bool same = dep[i] == want;
+                bool same = di == want;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const uint32_t expect = (pi < 0 ? 0u : msk[pi * 4 + w]) | ((i >> 5) == w ? 1u << (i & 31) : 0u);
-                    same = same && msk[i * 4 + w] == expect;
+                    same = same && mw[w] == expect;
                 }
                 if (!same) e = GDN_DEV_BAD_DESC;
-                else if (dep[i] > kMaxDepth) e = GDN_DEV_TOO_DEEP;
+                else if (di > kMaxDepth) e = GDN_DEV_TOO_DEEP;
             }
-            if (e) atomicOr(s_err, e);
+            if (e) atomicOr(&s_err[pp], e);
         }
-    }
-    __syncthreads();
-    if (*s_err) {
-        if (issuer) mbar_wait(&bar[B_KQ], 0);  // no TMA may land after the block exits
-        if (tid == 0) flag(p.status, *s_err);
-        __syncthreads();
-        tc_fence_before();
-        if (warp == 0) tmem_dealloc(tmem, 256);
-        return;
-    }
-
-    const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
-    // scatter of one half of the Gram: lane a holds k_a.k_i (cols 0..127) or
-    // k_a.q_i (cols 128..255) and writes them into the ancestor rows of its
-    // descendants i (the descendant bits of a come from its mask row).
-    auto scatter = [&](int col0, __half *dst, bool strict) {
-        const int a = row;
-        const int da = a < n ? dep[a] : 1;
-#pragma unroll 1
-        for (int cc = quad; cc < 4; ++cc) {
-            uint32_t dm = msk[a * 4 + cc];
-            if (strict && cc == quad) dm &= ~(1u << lane);  // X is strictly lower
-            if (!__any_sync(0xffffffffu, dm != 0u)) continue;
-            uint32_t v[32];
-            tmem_ld32_nowait(tmem + lane_base + col0 + cc * 32, v);
-            tmem_wait_ld_into(v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if ((dm >> c) & 1u) dst[(cc * 32 + c) * kMaxDepth + da - 1] = __float2half_rn(__uint_as_float(v[c]));
-        }
-    };
-
-    if (tree) {
-        // ===================== tree warps ======================================
-        const int i = tid;
-        const int myd = i < n ? dep[i] : 0;
-        // Gram: K [K;Q]^T -> columns [0, 256), issued by thread 0 once the tiles
-        // have landed: now if they have, else after the descendant rows
-        bool gram_issued = false;
-        auto issue_gram = [&]() {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t d = smem_desc(smem_u32(sm + OFF_KQ + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2);
-                mma_bf16(tmem, d, d, id_n256, ks > 0);
-            }
-            mma_commit(&bar[B_GRAM]);
-            gram_issued = true;
-        };
-        if (i == 0 && mbar_test(&bar[B_KQ], 0)) issue_gram();
-        // paths (the set bits of each mask row, root first) and gamma
-        if (i < n) {
+        // paths (the set bits of each mask row, root first; at most kMaxDepth
+        // entries even for a malformed row) and gamma
+        if (i < it.n) {
             float acc = 0.f;
             int l = 0;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                uint32_t word = msk[i * 4 + w];
-                while (word) {
+                uint32_t word = mw[w];
+                while (word && l < kMaxDepth) {
                     const int j = w * 32 + __ffs(word) - 1;
                     word &= word - 1;
                     path[i * kMaxDepth + l++] = (uint8_t)j;
@@ -313,103 +284,47 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         // block (its nodes i) x (word c of their ancestor rows), by five rounds of
         // shuffles (block transpose of Hacker's Delight, section 7-3, on
         // bit-reversed words so that bit c stands for column c); zero for c > w.
-        {
-            uint32_t anc[4], mine[4];
+        uint32_t mine[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                anc[c] = msk[i * 4 + c];
-                mine[c] = 0u;
+        for (int c = 0; c < 4; ++c) {
+            if (c > quad) break;  // warp-uniform
+            uint32_t x = __brev(mw[c]);
+            uint32_t m = 0x0000FFFFu;
+#pragma unroll
+            for (int j = 16; j != 0; j >>= 1, m ^= (m << j)) {
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, x, j);
+                x = (lane & j) ? x ^ (((other ^ (x >> j)) & m) << j) : x ^ ((x ^ (other >> j)) & m);
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c > quad) break;  // warp-uniform
-                uint32_t x = __brev(anc[c]);
-                uint32_t m = 0x0000FFFFu;
-#pragma unroll
-                for (int j = 16; j != 0; j >>= 1, m ^= (m << j)) {
-                    const uint32_t other = __shfl_xor_sync(0xffffffffu, x, j);
-                    x = (lane & j) ? x ^ (((other ^ (x >> j)) & m) << j) : x ^ ((x ^ (other >> j)) & m);
-                }
-                mine[c] = __brev(x);
-            }
-            named_sync(1, 128);  // every ancestor row has been read
-#pragma unroll
-            for (int c = 0; c < 4; ++c) msk[(c * 32 + lane) * 4 + quad] = mine[c];
+            mine[c] = __brev(x);
         }
-        const uint4 pr = *reinterpret_cast<const uint4 *>(path + i * kMaxDepth);
-        const uint32_t pw[4] = {pr.x, pr.y, pr.z, pr.w};
-        int node_at[kMaxDepth];
+        named_sync(1, 128);  // every ancestor row has been read by the validation
 #pragma unroll
-        for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0xFFu) : i;
-        if (i == 0 && !gram_issued) {
-            ok = mbar_wait(&bar[B_KQ], 0) && ok;
-            issue_gram();
-        }
+        for (int c = 0; c < 4; ++c) msk[(c * 32 + lane) * 4 + quad] = mine[c];
+        if (i == 0 && s_err[pp]) flag(p.status, s_err[pp]);
         named_sync(1, 128);
         mbar_arrive(&bar[B_DESC]);
+    };
 
-        // strict part of the Gram -> raw X rows
-        ok = mbar_wait(&bar[B_GRAM], 0) && ok;
-        tc_fence_after();
-        scatter(0, Xs, true);
-        tc_fence_before();
-        mbar_arrive(&bar[B_TFREE]);
-
-        // decay factors, X scaling, then P = Y (I + X)^-1 along the path
-        float dec[kMaxDepth];  // exp(gamma_i - gamma_path[l]); zero past the depth
-        const float gi = gam[i];
+    // State warps: S0 rows 32 sw .. 32 sw + 31 as bf16 (B operand, K-major,
+    // 128-byte swizzle), eight rows per batch, double-buffered; lane l holds
+    // columns 4l .. 4l + 3 (coalesced row reads).  Arrives on B_S0IN.
+    const int sw = warp - 4;
+    auto state_s0 = [&](const Item &it) {
+        const float *s0t = p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD);
+        float4 s0a[8], s0b[8];
+        auto s0_load = [&](float4 (&dst)[8], int batch) {
 #pragma unroll
-        for (int l = 0; l < kMaxDepth; ++l) dec[l] = l < myd ? expf(gi - gam[node_at[l]]) : 0.f;
-        ok = mbar_wait(&bar[B_TFREE], 0) && ok;  // every X and Y entry is in
-        {
-            const float bi = bet[i];
-            uint4 xw[2];
-            xw[0] = reinterpret_cast<const uint4 *>(Xs + i * kMaxDepth)[0];
-            xw[1] = reinterpret_cast<const uint4 *>(Xs + i * kMaxDepth)[1];
-            float xs[kMaxDepth];
+            for (int r = 0; r < 8; ++r)
+                dst[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (sw * 32 + batch * 8 + r) * kD) + lane);
+        };
+        auto s0_put = [&](const float4 (&src)[8], int batch) {
 #pragma unroll
-            for (int l = 0; l < kMaxDepth; ++l) xs[l] = half_at(xw, l) * bi * dec[l];
-            reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[0] =
-                make_uint4(pack_half(xs[0], xs[1]), pack_half(xs[2], xs[3]), pack_half(xs[4], xs[5]), pack_half(xs[6], xs[7]));
-            reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[1] =
-                make_uint4(pack_half(xs[8], xs[9]), pack_half(xs[10], xs[11]), pack_half(xs[12], xs[13]), pack_half(xs[14], xs[15]));
-        }
-        named_sync(1, 128);
-        float P[kMaxDepth];
-        {
-            uint4 yw[2];
-            yw[0] = reinterpret_cast<const uint4 *>(Ys + i * kMaxDepth)[0];
-            yw[1] = reinterpret_cast<const uint4 *>(Ys + i * kMaxDepth)[1];
-#pragma unroll
-            for (int l = 0; l < kMaxDepth; ++l) P[l] = dec[l] * half_at(yw, l);
-        }
-#pragma unroll
-        for (int a = kMaxDepth - 1; a >= 1; --a) {
-            // entries past the depth are zero, so a short path costs no branches
-            uint4 xw[2];
-            xw[0] = reinterpret_cast<const uint4 *>(Xs + node_at[a] * kMaxDepth)[0];
-            xw[1] = reinterpret_cast<const uint4 *>(Xs + node_at[a] * kMaxDepth)[1];
-            const float pa = a < myd ? P[a] : 0.f;
-#pragma unroll
-            for (int l = 0; l < a; ++l) P[l] = fmaf(-pa, half_at(xw, l), P[l]);
-        }
-        const float inv = 1.f / eg[i];
-
-        // P rows (A operand, K-major) once the K|Q space is free
-        ok = mbar_wait(&bar[B_S0], 0) && ok;
-        uint8_t *prow = sm + OFF_PA;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            *reinterpret_cast<uint4 *>(prow + sw128_offset(i, q * 8)) = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int l = 0; l < kMaxDepth; ++l)
-            if (l < myd)
-                *reinterpret_cast<__nv_bfloat16 *>(prow + sw128_offset(i, node_at[l])) = __float2bfloat16_rn(P[l] * inv);
-        fence_proxy_async_smem();
-        mbar_arrive(&bar[B_P]);
-    } else {
-        // ===================== state warps =====================================
-        // S0 as bf16 (B operand, K-major, 128B swizzle)
+            for (int r = 0; r < 8; ++r)
+                *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(sw * 32 + batch * 8 + r, 4 * lane)) =
+                    make_uint2(pack_bf16(src[r].x, src[r].y), pack_bf16(src[r].z, src[r].w));
+        };
+        s0_load(s0a, 0);
+        s0_load(s0b, 1);
         s0_put(s0a, 0);
         s0_load(s0a, 2);
         s0_put(s0b, 1);
@@ -418,154 +333,328 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         s0_put(s0b, 3);
         fence_proxy_async_smem();
         mbar_arrive(&bar[B_S0IN]);
+    };
 
-        // full part of the Gram -> raw Y rows
-        ok = mbar_wait(&bar[B_DESC], 0) && ok;
-        ok = mbar_wait(&bar[B_GRAM], 0) && ok;
-        tc_fence_after();
-        scatter(128, Ys, false);
-        tc_fence_before();
-        mbar_arrive(&bar[B_TFREE]);
+    // scatter of one half of the Gram: lane a holds k_a.k_i (cols 0..127) or
+    // k_a.q_i (cols 128..255) and writes them into the ancestor rows of its
+    // descendants i (the descendant bits of a come from its mask row).
+    auto scatter = [&](int col0, __half *dst, bool strict) {
+        const int a = row;
+        const int da = a < cur.n ? min(max(dep[a], 1), kMaxDepth) : 1;
+#pragma unroll 1
+        for (int cc = quad; cc < 4; ++cc) {
+            uint32_t dm = msk[a * 4 + cc];
+            if (strict && cc == quad) dm &= ~(1u << lane);  // X is strictly lower
+            if (!__any_sync(0xffffffffu, dm != 0u)) continue;
+            uint32_t v[32];
+            tmem_ld32_nowait(tmem + lane_base + col0 + cc * 32, v);
+            tmem_wait_ld_into(v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if ((dm >> c) & 1u) dst[(cc * 32 + c) * kMaxDepth + da - 1] = __float2half_rn(__uint_as_float(v[c]));
+        }
+    };
 
+    // ---- the first item's operands -------------------------------------------
+    if (issuer) issue_kq(cur);
+    if (tree) tree_meta(cur, 0);
+    else state_s0(cur);
+
+    const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
+    for (int it = 0;; ++it) {
+        const int ph = it & 1;
+        const int n = cur.n, nb = (n + 31) >> 5;
+        // the next item: its offsets are read now, used near the end of this one
+        const int cand = cur.idx + gridDim.x;
+        int c_lo = 0, c_hi = 0;
+        if (cand < p.items) {
+            c_lo = __ldg(p.offsets + cand / p.hv_n);
+            c_hi = __ldg(p.offsets + cand / p.hv_n + 1);
+        }
         if (issuer) {
-            // S0 part: W = K S0^T (cols 0..127), Z = Q S0^T (cols 128..255)
-            ok = mbar_wait(&bar[B_S0IN], 0) && ok;
-            ok = mbar_wait(&bar[B_TFREE], 0) && ok;
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kq = smem_u32(sm + OFF_KQ + (ks >> 2) * 32768 + (ks & 3) * 32);
-                const uint64_t bs = smem_desc(smem_u32(sm + OFF_S0 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-                mma_bf16(tmem, smem_desc(kq, 16, 1024, 2), bs, id_n128, ks > 0);
-                mma_bf16(tmem + 128, smem_desc(kq + 16384, 16, 1024, 2), bs, id_n128, ks > 0);
-            }
-            mma_commit(&bar[B_S0]);
-            // V tile into the S0 space once those MMAs are done
-            ok = mbar_wait(&bar[B_S0], 0) && ok;
-            mbar_arrive_expect_tx(&bar[B_V], (uint32_t)(2 * nbox * 4096));
+            // L2 hints: the next item's S0 tile and this item's V tile
+            if (cand < p.items) prefetch_l2(p.S0 + (int64_t)cand * (kD * kD), kD * kD * 4);
             for (int h = 0; h < 2; ++h)
-                for (int r = 0; r < nbox; ++r)
-                    tma_load_3d(sm + OFF_S0 + h * 16384 + r * 4096, &tmV, &bar[B_V], h * 64, hv, lo + 32 * r);
+                for (int r = 0; r < nb; ++r) tma_prefetch_3d(&tmV, h * 64, cur.hv, cur.lo + 32 * r);
         }
-
-        // right-hand side rows R[j][n] = beta_j v[j][n] - beta_j e^gamma_j W[j][n] (MN-major B).
-        // A row with a non-finite entry is stored as zero (its subtree's outputs are
-        // set to NaN), and so is every row past the tree.
-        const int j = row;
-        ok = mbar_wait(&bar[B_V], 0) && ok;
-        tc_fence_after();
-        const float bj = bet[j], bej = bj * egt[j];
-        float chk = 0.f;  // 0 * x: stays zero while every entry is finite
-        auto r_chunk = [&](const uint32_t (&w)[32], int cc) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n0 = cc * 32 + q * 8;
-                const uint4 vv = *reinterpret_cast<const uint4 *>(sm + OFF_S0 + sw128_offset(j, n0));
-                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-                float r[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float vj = (e & 1) ? bf16_hi(vw[e >> 1]) : bf16_lo(vw[e >> 1]);
-                    r[e] = fmaf(-bej, __uint_as_float(w[q * 8 + e]), bj * vj);
-                    chk = fmaf(0.f, r[e], chk);
-                }
-                *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, n0)) =
-                    make_uint4(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]), pack_bf16(r[4], r[5]), pack_bf16(r[6], r[7]));
+        auto next = [&](Item &nx) -> bool {
+            if (cand >= p.items) return false;
+            if (item_ok(c_lo, c_hi - c_lo, p.total)) {
+                set_item(p, cand, c_lo, c_hi - c_lo, nx);
+                return true;
             }
+            return find_item(p, cand, gridDim.x, tid == 0, nx);
         };
-        {
-            // W columns 32 at a time, the next load in flight while one is used
-            uint32_t wa[32], wb[32];
-            tmem_ld32_nowait(tmem + lane_base, wa);
-            tmem_wait_ld_into(wa);
-            tmem_ld32_nowait(tmem + lane_base + 32, wb);
-            r_chunk(wa, 0);
-            tmem_wait_ld_into(wb);
-            tmem_ld32_nowait(tmem + lane_base + 64, wa);
-            r_chunk(wb, 1);
-            tmem_wait_ld_into(wa);
-            tmem_ld32_nowait(tmem + lane_base + 96, wb);
-            r_chunk(wa, 2);
-            tmem_wait_ld_into(wb);
-            r_chunk(wb, 3);
-        }
-        const bool bad = chk != 0.f;
-        if (bad || j >= n) {
+
+        if (tree) {
+            // ===================== tree warps ==================================
+            const int i = tid;
+            const int myd = i < n ? min(dep[i], kMaxDepth) : 0;
+            if (i == 0) {
+                // Gram: K [K;Q]^T -> columns [0, 256), once the tiles have landed
+                // and the previous item's Z has been read out
+                if (it > 0) ok = mbar_wait(&bar[B_ZFREE], ph ^ 1) && ok;
+                ok = mbar_wait(&bar[B_KQ], ph) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t d = smem_desc(smem_u32(sm + OFF_KQ + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2);
+                    mma_bf16(tmem, d, d, id_n256, ks > 0);
+                }
+                mma_commit(&bar[B_GRAM]);
+            }
+            const uint4 pr = *reinterpret_cast<const uint4 *>(path + i * kMaxDepth);
+            const uint32_t pw[4] = {pr.x, pr.y, pr.z, pr.w};
+            int node_at[kMaxDepth];
+#pragma unroll
+            for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0x7Fu) : i;
+
+            // strict part of the Gram -> raw X rows
+            ok = mbar_wait(&bar[B_GRAM], ph) && ok;
+            tc_fence_after();
+            scatter(0, Xs, true);
+            tc_fence_before();
+            mbar_arrive(&bar[B_TFREE]);
+
+            // decay factors, X scaling, then P = Y (I + X)^-1 along the path
+            float dec[kMaxDepth];  // exp(gamma_i - gamma_path[l]); zero past the depth
+            const float gi = gam[i];
+#pragma unroll
+            for (int l = 0; l < kMaxDepth; ++l) dec[l] = l < myd ? expf(gi - gam[node_at[l]]) : 0.f;
+            ok = mbar_wait(&bar[B_TFREE], ph) && ok;  // every X and Y entry is in
+            {
+                const float bi = bet[i];
+                uint4 xw[2];
+                xw[0] = reinterpret_cast<const uint4 *>(Xs + i * kMaxDepth)[0];
+                xw[1] = reinterpret_cast<const uint4 *>(Xs + i * kMaxDepth)[1];
+                float xs[kMaxDepth];
+#pragma unroll
+                for (int l = 0; l < kMaxDepth; ++l) xs[l] = half_at(xw, l) * bi * dec[l];
+                reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[0] =
+                    make_uint4(pack_half(xs[0], xs[1]), pack_half(xs[2], xs[3]), pack_half(xs[4], xs[5]), pack_half(xs[6], xs[7]));
+                reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[1] =
+                    make_uint4(pack_half(xs[8], xs[9]), pack_half(xs[10], xs[11]), pack_half(xs[12], xs[13]), pack_half(xs[14], xs[15]));
+            }
+            named_sync(1, 128);
+            float P[kMaxDepth];
+            {
+                uint4 yw[2];
+                yw[0] = reinterpret_cast<const uint4 *>(Ys + i * kMaxDepth)[0];
+                yw[1] = reinterpret_cast<const uint4 *>(Ys + i * kMaxDepth)[1];
+#pragma unroll
+                for (int l = 0; l < kMaxDepth; ++l) P[l] = dec[l] * half_at(yw, l);
+            }
+#pragma unroll
+            for (int a = kMaxDepth - 1; a >= 1; --a) {
+                // entries past the depth are zero, so a short path costs no branches
+                uint4 xw[2];
+                xw[0] = reinterpret_cast<const uint4 *>(Xs + node_at[a] * kMaxDepth)[0];
+                xw[1] = reinterpret_cast<const uint4 *>(Xs + node_at[a] * kMaxDepth)[1];
+                const float pa = a < myd ? P[a] : 0.f;
+#pragma unroll
+                for (int l = 0; l < a; ++l) P[l] = fmaf(-pa, half_at(xw, l), P[l]);
+            }
+            const float inv = 1.f / eg[i];
+
+            // P rows (A operand, K-major) once the K|Q space is free
+            ok = mbar_wait(&bar[B_S0], ph) && ok;
+            uint8_t *prow = sm + OFF_PA;
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, q * 8)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (bad && j < n) {  // the row and every node below it
+                *reinterpret_cast<uint4 *>(prow + sw128_offset(i, q * 8)) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) atomicOr(&pset[w], msk[j * 4 + w]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bar[B_R]);
-
-        // output: Z += (e^-gamma' P) R
-        if (issuer) {
-            ok = mbar_wait(&bar[B_R], 0) && ok;
-            ok = mbar_wait(&bar[B_P], 0) && ok;
-            tc_fence_after();
-            const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = smem_desc(smem_u32(sm + OFF_PA + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-                const uint64_t bd = smem_desc(smem_u32(sm + OFF_RB + ks * 2048), 16384, 1024, 2);
-                mma_bf16(tmem + 128, ad, bd, id_out, true);
-            }
-            mma_commit(&bar[B_OUT]);
-        }
-
-        // epilogue: o[i][n] = scale * e^gamma'_i * Z[i][n]; each row is staged in
-        // the K|Q space (row stride padded by 16 bytes, so the 32 rows of a warp
-        // hit distinct banks) and leaves as one bulk copy
-        ok = mbar_wait(&bar[B_OUT], 0) && ok;
-        ok = mbar_wait(&bar[B_R], 0) && ok;  // every poisoned row is marked
-        tc_fence_after();
-        const int i = row;
-        const bool hit = (pset[i >> 5] >> (i & 31)) & 1u;
-        const float f = hit ? __int_as_float(0x7fc00000) : p.scale * eg[i];  // NaN * z is NaN
-        constexpr int kRowBytes = kD * (int)sizeof(Tout);
-        uint8_t *srow = sm + OFF_KQ + i * (kRowBytes + 16);
-        auto o_chunk = [&](const uint32_t (&zr)[32], int cc) {
-            float z[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) z[e] = f * __uint_as_float(zr[e]);
-            if constexpr (sizeof(Tout) == 2) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(srow + (cc * 4 + q) * 16) =
-                        make_uint4(pack_bf16(z[q * 8 + 0], z[q * 8 + 1]), pack_bf16(z[q * 8 + 2], z[q * 8 + 3]),
-                                   pack_bf16(z[q * 8 + 4], z[q * 8 + 5]), pack_bf16(z[q * 8 + 6], z[q * 8 + 7]));
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4 *>(srow + (cc * 8 + q) * 16) =
-                        make_float4(z[q * 4 + 0], z[q * 4 + 1], z[q * 4 + 2], z[q * 4 + 3]);
-            }
-        };
-        {
-            uint32_t za[32], zb[32];
-            tmem_ld32_nowait(tmem + lane_base + 128, za);
-            tmem_wait_ld_into(za);
-            tmem_ld32_nowait(tmem + lane_base + 160, zb);
-            o_chunk(za, 0);
-            tmem_wait_ld_into(zb);
-            tmem_ld32_nowait(tmem + lane_base + 192, za);
-            o_chunk(zb, 1);
-            tmem_wait_ld_into(za);
-            tmem_ld32_nowait(tmem + lane_base + 224, zb);
-            o_chunk(za, 2);
-            tmem_wait_ld_into(zb);
-            o_chunk(zb, 3);
-        }
-        if (i < n) {
+            for (int l = 0; l < kMaxDepth; ++l)
+                if (l < myd)
+                    *reinterpret_cast<__nv_bfloat16 *>(prow + sw128_offset(i, node_at[l])) = __float2bfloat16_rn(P[l] * inv);
             fence_proxy_async_smem();
-            bulk_store(static_cast<uint8_t *>(p.o) + ((int64_t)(lo + i) * p.hv_n + hv) * kRowBytes, srow, kRowBytes);
-            bulk_commit();
-            bulk_wait_read();
+            mbar_arrive(&bar[B_P]);
+
+            // the next item's tree data, once the state warps hold this item's
+            Item nx;
+            if (!next(nx)) break;
+            ok = mbar_wait(&bar[B_META], ph) && ok;
+            tree_meta(nx, ph ^ 1);
+            cur = nx;
+        } else {
+            // ===================== state warps =================================
+            // full part of the Gram -> raw Y rows
+            ok = mbar_wait(&bar[B_DESC], ph) && ok;
+            ok = mbar_wait(&bar[B_GRAM], ph) && ok;
+            tc_fence_after();
+            scatter(128, Ys, false);
+            tc_fence_before();
+            mbar_arrive(&bar[B_TFREE]);
+
+            if (issuer) {
+                // S0 part: W = K S0^T (cols 0..127), Z = Q S0^T (cols 128..255)
+                ok = mbar_wait(&bar[B_S0IN], ph) && ok;
+                ok = mbar_wait(&bar[B_TFREE], ph) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kq = smem_u32(sm + OFF_KQ + (ks >> 2) * 32768 + (ks & 3) * 32);
+                    const uint64_t bs = smem_desc(smem_u32(sm + OFF_S0 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
+                    mma_bf16(tmem, smem_desc(kq, 16, 1024, 2), bs, id_n128, ks > 0);
+                    mma_bf16(tmem + 128, smem_desc(kq + 16384, 16, 1024, 2), bs, id_n128, ks > 0);
+                }
+                mma_commit(&bar[B_S0]);
+                // V tile into the S0 space once those MMAs are done
+                ok = mbar_wait(&bar[B_S0], ph) && ok;
+                mbar_arrive_expect_tx(&bar[B_V], (uint32_t)(2 * nb * 4096));
+                for (int h = 0; h < 2; ++h)
+                    for (int r = 0; r < nb; ++r)
+                        tma_load_3d(sm + OFF_S0 + h * 16384 + r * 4096, &tmV, &bar[B_V], h * 64, cur.hv, cur.lo + 32 * r);
+            }
+
+            // this item's per-row data into registers; the tree warps may then
+            // overwrite it with the next item's
+            const int j = row;
+            const float bj = bet[j], bej = bj * egt[j];
+            const float f_out = p.scale * eg[j];
+            uint32_t desc_row[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) desc_row[w] = msk[j * 4 + w];
+            const bool item_good = s_err[ph] == 0;
+            const bool store = item_good && j < n;
+            mbar_arrive(&bar[B_META]);
+
+            // right-hand side rows R[j][n] = beta_j v[j][n] - beta_j e^gamma_j W[j][n] (MN-major B).
+            // A row with a non-finite entry is stored as zero (its subtree's outputs are
+            // set to NaN), and so is every row past the tree.
+            ok = mbar_wait(&bar[B_V], ph) && ok;
+            tc_fence_after();
+            float chk = 0.f;  // 0 * x: stays zero while every entry is finite
+            auto r_chunk = [&](const uint32_t (&w)[32], int cc) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int n0 = cc * 32 + q * 8;
+                    const uint4 vv = *reinterpret_cast<const uint4 *>(sm + OFF_S0 + sw128_offset(j, n0));
+                    const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+                    float r[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float vj = (e & 1) ? bf16_hi(vw[e >> 1]) : bf16_lo(vw[e >> 1]);
+                        r[e] = fmaf(-bej, __uint_as_float(w[q * 8 + e]), bj * vj);
+                        chk = fmaf(0.f, r[e], chk);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, n0)) =
+                        make_uint4(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]), pack_bf16(r[4], r[5]), pack_bf16(r[6], r[7]));
+                }
+            };
+            {
+                // W columns 32 at a time, the next load in flight while one is used
+                uint32_t wa[32], wb[32];
+                tmem_ld32_nowait(tmem + lane_base, wa);
+                tmem_wait_ld_into(wa);
+                tmem_ld32_nowait(tmem + lane_base + 32, wb);
+                r_chunk(wa, 0);
+                tmem_wait_ld_into(wb);
+                tmem_ld32_nowait(tmem + lane_base + 64, wa);
+                r_chunk(wb, 1);
+                tmem_wait_ld_into(wa);
+                tmem_ld32_nowait(tmem + lane_base + 96, wb);
+                r_chunk(wa, 2);
+                tmem_wait_ld_into(wb);
+                r_chunk(wb, 3);
+            }
+            const bool bad = chk != 0.f;
+            if (bad || j >= n) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    *reinterpret_cast<uint4 *>(sm + OFF_RB + sw128_offset(j, q * 8)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (bad && j < n) {  // the row and every node below it
+#pragma unroll
+                for (int w = 0; w < 4; ++w) atomicOr(&pset[ph * 4 + w], desc_row[w]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_R]);
+
+            Item nx;
+            const bool more = next(nx);
+            // output: Z += (e^-gamma' P) R
+            if (issuer) {
+                ok = mbar_wait(&bar[B_R], ph) && ok;
+                ok = mbar_wait(&bar[B_P], ph) && ok;
+                tc_fence_after();
+                const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = smem_desc(smem_u32(sm + OFF_PA + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
+                    const uint64_t bd = smem_desc(smem_u32(sm + OFF_RB + ks * 2048), 16384, 1024, 2);
+                    mma_bf16(tmem + 128, ad, bd, id_out, true);
+                }
+                mma_commit(&bar[B_OUT]);
+            }
+            ok = mbar_wait(&bar[B_OUT], ph) && ok;  // also: every R row (and V read) is done
+            tc_fence_after();
+            if (issuer && more) issue_kq(nx);       // the K|Q space is free again
+
+            // epilogue: o[i][n] = scale * e^gamma'_i * Z[i][n], NaN for a poisoned row.
+            // bf16 rows of whole 32-node boxes are staged in the S0 space (free once
+            // every R row is built) in the 128-byte-swizzled box layout and leave by
+            // TMA; rows of a ragged last box, and fp32 rows, are stored directly.
+            const int i = row;
+            const bool hit = (pset[ph * 4 + (i >> 5)] >> (i & 31)) & 1u;
+            const float f = hit ? __int_as_float(0x7fc00000) : f_out;  // NaN * z is NaN
+            const int nfull = n & ~31;
+            const bool staged = sizeof(Tout) == 2 && i < nfull;
+            Tout *orow = static_cast<Tout *>(p.o) + ((int64_t)(cur.lo + i) * p.hv_n + cur.hv) * kD;
+            auto o_chunk = [&](const uint32_t (&zr)[32], int cc) {
+                float z[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) z[e] = f * __uint_as_float(zr[e]);
+                if (!store) return;
+                if constexpr (sizeof(Tout) == 2) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w = make_uint4(pack_bf16(z[q * 8 + 0], z[q * 8 + 1]), pack_bf16(z[q * 8 + 2], z[q * 8 + 3]),
+                                                   pack_bf16(z[q * 8 + 4], z[q * 8 + 5]), pack_bf16(z[q * 8 + 6], z[q * 8 + 7]));
+                        if (staged)
+                            *reinterpret_cast<uint4 *>(sm + OFF_S0 + sw128_offset(i, cc * 32 + q * 8)) = w;
+                        else
+                            reinterpret_cast<uint4 *>(orow + cc * 32)[q] = w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        reinterpret_cast<float4 *>(orow + cc * 32)[q] =
+                            make_float4(z[q * 4 + 0], z[q * 4 + 1], z[q * 4 + 2], z[q * 4 + 3]);
+                }
+            };
+            {
+                uint32_t za[32], zb[32];
+                tmem_ld32_nowait(tmem + lane_base + 128, za);
+                tmem_wait_ld_into(za);
+                tmem_ld32_nowait(tmem + lane_base + 160, zb);
+                o_chunk(za, 0);
+                tmem_wait_ld_into(zb);
+                tmem_ld32_nowait(tmem + lane_base + 192, za);
+                o_chunk(zb, 1);
+                tmem_wait_ld_into(za);
+                tmem_ld32_nowait(tmem + lane_base + 224, zb);
+                o_chunk(za, 2);
+                tmem_wait_ld_into(zb);
+                o_chunk(zb, 3);
+            }
+            tc_fence_before();
+            mbar_arrive(&bar[B_ZFREE]);
+            if constexpr (sizeof(Tout) == 2) {
+                fence_proxy_async_smem();  // staged rows are visible to the TMA engine
+                named_sync(2, 128);
+                if (issuer && item_good && nfull > 0) {
+                    for (int h = 0; h < 2; ++h)
+                        for (int r = 0; r < (nfull >> 5); ++r)
+                            tma_store_3d(&tmO, sm + OFF_S0 + h * 16384 + r * 4096, h * 64, cur.hv, cur.lo + 32 * r);
+                    bulk_commit();
+                    bulk_wait_read();
+                }
+                named_sync(2, 128);  // the S0 space may be written again
+            }
+            if (!more) break;
+            state_s0(nx);
+            cur = nx;
         }
     }
     if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
@@ -599,28 +688,35 @@ bool verify_tc_supported(const gdn_verify_args &a) {
 }
 
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream) {
-    CUtensorMap tmK, tmQ, tmV;
+    CUtensorMap tmK, tmQ, tmV, tmO;
     if (!encode_tokens(&tmK, a.k, a.n_k_heads, a.total_nodes) ||
         !encode_tokens(&tmQ, a.q, a.n_k_heads, a.total_nodes) ||
         !encode_tokens(&tmV, a.v, a.n_v_heads, a.total_nodes))
         return cudaErrorInvalidValue;
+    // bf16 outputs leave through TMA stores of the same box shape as V
+    if (a.out_dtype == GDN_BF16) {
+        if (!encode_tokens(&tmO, a.o, a.n_v_heads, a.total_nodes)) return cudaErrorInvalidValue;
+    } else {
+        tmO = tmV;  // unused by the fp32-output kernel
+    }
     TcParams p;
     p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.words = a.mask_words < 4 ? a.mask_words : 4;
-    p.total = a.total_nodes; p.scale = a.scale;
+    p.total = a.total_nodes; p.items = a.batch * a.n_v_heads; p.scale = a.scale;
     p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth; p.mask = a.anc_mask;
-    p.v = static_cast<const __nv_bfloat16 *>(a.v); p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
+    p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
     p.o = a.o; p.status = a.dev_status;
-    const dim3 grid((unsigned)a.batch * (unsigned)a.n_v_heads);
+    // persistent: two blocks per SM (tensor memory and shared memory allow two)
+    const dim3 grid((unsigned)std::min(p.items, 2 * sm_count()));
     cudaError_t e;
     if (a.out_dtype == GDN_BF16) {
         e = cudaFuncSetAttribute(verify_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
         if (e != cudaSuccess) return e;
-        verify_tc_kernel<__nv_bfloat16><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, p);
+        verify_tc_kernel<__nv_bfloat16><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, tmO, p);
     } else {
         e = cudaFuncSetAttribute(verify_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        verify_tc_kernel<float><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, p);
+        verify_tc_kernel<float><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, tmO, p);
     }
     return cudaGetLastError();
 }

@@ -331,7 +331,8 @@ def test_bad_path_sets_status_and_leaves_state(path):
 
 def _tc_batch(seed, sizes, hk=2, hv=4, max_depth=16, fn=None):
     rng = np.random.default_rng(seed)
-    parents = [fn(rng, n) if fn else W.depth_capped_random_tree(rng, n, max_depth) for n in sizes]
+    parents = [np.zeros(0, np.int32) if n == 0 else fn(rng, n) if fn
+               else W.depth_capped_random_tree(rng, n, max_depth) for n in sizes]
     tb = W.custom(seed, parents, n_k_heads=hk, n_v_heads=hv, d=128, qkv_dtype="bf16")
     tb.max_depth_bound = 16
     return tb
@@ -401,6 +402,43 @@ def test_tc_path_non_finite_inputs_stay_on_their_branch():
             o2, st2, _ = run_verify(tb2)
             gb.check_status(st2)
             assert torch.equal(o2[keep], base[keep])
+
+
+def _mixed_sizes(count):
+    cycle = (0, 1, 33, 128, 7, 64, 100, 2)
+    return tuple(cycle[i % len(cycle)] for i in range(count))
+
+
+def test_tc_path_many_items_per_block():
+    # 240 requests x 4 value heads: more items than resident blocks, so each
+    # persistent block runs several items of mixed sizes (and skips empty ones)
+    tb = _tc_batch(21, _mixed_sizes(240))
+    o, status, _ = run_verify(tb)
+    gb.check_status(status)
+    assert rel_err(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_tc_path_bad_request_among_many_is_skipped():
+    tb = _tc_batch(22, _mixed_sizes(240))
+    d = gb.upload(tb)
+    status = gb.new_status()
+    mask, depth = run_desc(d, tb, status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    bad = 11                                   # a request of 128 nodes
+    lo, hi = int(tb.node_offsets[bad]), int(tb.node_offsets[bad + 1])
+    depth[lo + 5] += 1                         # stale descriptor row
+    out = torch.full((tb.total_nodes, tb.n_v_heads, tb.d_v), 5.0, dtype=torch.bfloat16,
+                     device=d["q"].device)
+    gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                       d["parent"], mask, depth, tb.max_nodes, max_depth=16, out=out,
+                       dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 32
+    assert torch.all(out[lo:hi] == 5.0)        # the malformed request is skipped
+    ref = oracle.verify(tb)
+    keep = np.r_[0:lo, hi:tb.total_nodes]
+    assert rel_err(out.float().cpu().numpy()[keep], ref[keep]) <= TOL_BF16
 
 
 def test_tc_path_leaves_S0_untouched():
