@@ -8,8 +8,10 @@
 //     S_new = e^gamma_L S0 + sum_t e^(gamma_L - gamma_t) u_t k_t^T
 // which equals running the gated delta rule along the path.
 //
-// One block per (request, value head).  Both contractions are GEMMs with a
-// 16-wide side and run on tcgen05 with fp32 accumulation:
+// Persistent blocks (two per SM) walk the (request, value head) items; the next
+// item's state tile is requested into L2 while the current one is committed.
+// Both contractions are GEMMs with a 16-wide side and run on tcgen05 with fp32
+// accumulation:
 //     W  = S0 K^T      M = 128 state rows, N = 16 path keys, K = 128
 //     U  = A K         M = 128 state rows, N = 128 columns,  K = 16 path keys
 // where A[row][t] = e^(gamma_L - gamma_t) u_t[row].  The fp32 operands S0 and
@@ -17,6 +19,8 @@
 // are exact in bf16, so both products keep fp32 accuracy.  The chain solve for
 // u runs per state row in registers.  The state tile moves by TMA both ways and
 // is fully read before it is overwritten, so S_new may alias S0.
+#include <algorithm>
+
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -37,12 +41,13 @@ constexpr int OFF_A = OFF_KEYS + 4096;  // A hi | lo: bf16 [128][16] core-matrix
 constexpr int OFF_VP = OFF_A + 8192;    // fp32 path values [16][128]
 constexpr int OFF_COEF = OFF_VP + kMaxPath * kD * 4;  // fp32 [16][16]
 constexpr int OFF_SCAL = OFF_COEF + kMaxPath * kMaxPath * 4;  // bet, egam, fdec, gam [16]; pn [16]
-constexpr int OFF_MISC = OFF_SCAL + 5 * kMaxPath * 4;       // tmem slot, bad
+constexpr int OFF_MISC = OFF_SCAL + 5 * kMaxPath * 4;       // tmem slot, bad path flags [2]
 constexpr int OFF_BAR = OFF_MISC + 16;
 constexpr int kSmemBytes = OFF_BAR + 3 * 8;
 
 struct TcCommitParams {
-    int hk_n, hv_n, total;
+    int hk_n, hv_n, total, items;
+    const float *S0;
     const int32_t *offsets, *parent, *poff, *pidx;
     const __nv_bfloat16 *k, *v;
     const float *g, *beta;
@@ -84,221 +89,240 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);  // tile, W, U
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
-    const int hv = blockIdx.x % p.hv_n, b = blockIdx.x / p.hv_n;
-    const int hk = hv / (p.hv_n / p.hk_n);
-    const int lo = p.offsets[b];
-    const int n = p.offsets[b + 1] - lo;
-    const int pa = p.poff[b];
-    const int L = p.poff[b + 1] - pa;
-    const int tile_row = blockIdx.x * kD;
     if ((smem_u32(sm) & 1023u) != 0u) {
         if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
         return;
     }
-    if (L < 0 || L > kMaxPath || L > n || lo < 0 || lo + n > p.total) {
-        if (tid == 0) flag(p.status, L > kMaxPath && L <= n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
-        return;
-    }
+    if ((int)blockIdx.x >= p.items) return;
     const int row = quad * 32 + lane, half = warp >> 2;  // tensor-memory lane = state row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     if (tid == 0) {
         for (int k = 0; k < 3; ++k) mbar_init(&bar[k], 1);
         fence_mbar_init();
-        *s_bad = 0;
-        mbar_arrive_expect_tx(&bar[0], kD * kD * 4);
-        for (int q = 0; q < 4; ++q) tma_load_2d(tile + q * kD * 32, &tmS0, &bar[0], q * 32, tile_row);
+        s_bad[0] = s_bad[1] = 0;
     }
     if (warp == 0) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    // path validation
-    if (tid < L) {
-        const int node = p.pidx[pa + tid];
-        const int expect = tid == 0 ? -1 : p.pidx[pa + tid - 1];
-        pn[tid] = node;
-        if (node < 0 || node >= n || p.parent[lo + node] != expect) atomicOr(s_bad, 1);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const bool bad = *s_bad != 0;
+    bool ok = true;
+    uint32_t ph_tile = 0, ph_mma = 0;  // completed phases of the tile and MMA barriers
+    int it = 0;                        // items committed by this block
 
-    // path keys (bf16, 16-byte pieces; rows past L are zero) and values (fp32)
-    {
-        const int t = tid >> 4, c = tid & 15;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-        if (!bad && t < L) {
-            const int64_t node = lo + pn[t];
-            kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (node * p.hk_n + hk) * kD) + c);
-            vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (node * p.hv_n + hv) * kD) + c);
+    for (int idx = blockIdx.x; idx < p.items; idx += gridDim.x) {
+        const int hv = idx % p.hv_n, b = idx / p.hv_n;
+        const int hk = hv / (p.hv_n / p.hk_n);
+        const int lo = p.offsets[b];
+        const int n = p.offsets[b + 1] - lo;
+        const int pa = p.poff[b];
+        const int L = p.poff[b + 1] - pa;
+        const int tile_row = idx * kD;
+        if (L < 0 || L > kMaxPath || L > n || lo < 0 || lo + n > p.total) {
+            if (tid == 0) flag(p.status, L > kMaxPath && L <= n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
+            continue;
         }
-        *reinterpret_cast<uint4 *>(sm + OFF_KEYS + sw128(t, c * 8, kMaxPath)) = kv;
-        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
-        float *vrow = vp + t * kD + c * 8;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            vrow[2 * e] = __uint_as_float(w[e] << 16);
-            vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        int *bad_flag = s_bad + (it & 1);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar[0], kD * kD * 4);
+            for (int q = 0; q < 4; ++q) tma_load_2d(tile + q * kD * 32, &tmS0, &bar[0], q * 32, tile_row);
+            if (idx + (int)gridDim.x < p.items)  // the next item's state tile, into L2
+                prefetch_l2(p.S0 + (int64_t)(idx + gridDim.x) * (kD * kD), kD * kD * 4);
         }
-        if (!bad && tid < L) {
-            const int64_t node = lo + pn[tid];
-            gam[tid] = p.g[node * p.hv_n + hv];
-            bet[tid] = p.beta[node * p.hv_n + hv];
+        // path validation
+        if (tid < L) {
+            const int node = p.pidx[pa + tid];
+            const int expect = tid == 0 ? -1 : p.pidx[pa + tid - 1];
+            pn[tid] = node;
+            if (node < 0 || node >= n || p.parent[lo + node] != expect) atomicOr(bad_flag, 1);
         }
-    }
-    __syncthreads();
-    if (tid == 0 && !bad) {
-        float acc = 0.f;
-        for (int t = 0; t < L; ++t) {
-            acc += gam[t];
-            gam[t] = acc;
-            egam[t] = expf(acc);
-        }
-        for (int t = 0; t < L; ++t) fdec[t] = expf(acc - gam[t]);
-    }
-    __syncthreads();
-    // chain coefficients beta_t e^(gamma_t - gamma_s) (k_t . k_s): one warp per pair
-    if (!bad) {
-        for (int pr = warp; pr < L * (L - 1) / 2; pr += kT / 32) {
-            int t = 1, base = 0;
-            while (base + t <= pr) { base += t; ++t; }
-            const int s = pr - base;
-            float d = 0.f;
+        __syncthreads();
+        const bool bad = *bad_flag != 0;
+        if (tid == 0) s_bad[(it & 1) ^ 1] = 0;  // the next item's flag starts clear
+
+        // path keys (bf16, 16-byte pieces; rows past L are zero) and values (fp32)
+        {
+            const int t = tid >> 4, c = tid & 15;
+            uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+            if (!bad && t < L) {
+                const int64_t node = lo + pn[t];
+                kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (node * p.hk_n + hk) * kD) + c);
+                vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (node * p.hv_n + hv) * kD) + c);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_KEYS + sw128(t, c * 8, kMaxPath)) = kv;
+            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+            float *vrow = vp + t * kD + c * 8;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int m = lane * 4 + e;
-                d = fmaf(bf16_at(sm + OFF_KEYS, sw128(t, m, kMaxPath)), bf16_at(sm + OFF_KEYS, sw128(s, m, kMaxPath)), d);
+                vrow[2 * e] = __uint_as_float(w[e] << 16);
+                vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
             }
-            d = warp_sum(d);
-            if (lane == 0) coef[t * kMaxPath + s] = bet[t] * expf(gam[t] - gam[s]) * d;
-        }
-    }
-
-    // the state tile: row, columns 64 half .. 64 half + 63 into registers
-    bool ok = mbar_wait(&bar[0], 0);
-    float s[64];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const float4 x = *reinterpret_cast<const float4 *>(tile + tile_index(row, half * 64 + c * 4));
-        s[c * 4 + 0] = x.x; s[c * 4 + 1] = x.y; s[c * 4 + 2] = x.z; s[c * 4 + 3] = x.w;
-    }
-    __syncthreads();  // every thread holds its part; the tile space becomes S0 hi | lo
-    if (!bad) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            float hi[8], lw[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                hi[e] = __bfloat162float(__float2bfloat16_rn(s[c * 8 + e]));
-                lw[e] = s[c * 8 + e] - hi[e];
+            if (!bad && tid < L) {
+                const int64_t node = lo + pn[tid];
+                gam[tid] = p.g[node * p.hv_n + hv];
+                bet[tid] = p.beta[node * p.hv_n + hv];
             }
-            const uint32_t off = sw128(row, half * 64 + c * 8, kD);
-            *reinterpret_cast<uint4 *>(sm + OFF_TILE + off) =
-                make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-            *reinterpret_cast<uint4 *>(sm + OFF_TILE + 32768 + off) =
-                make_uint4(pack_bf16(lw[0], lw[1]), pack_bf16(lw[2], lw[3]), pack_bf16(lw[4], lw[5]), pack_bf16(lw[6], lw[7]));
         }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    if (!bad) {
-        // W = S0 K^T (hi + lo) -> tensor-memory columns [0, 16)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 16);
+        __syncthreads();
+        if (tid == 0 && !bad) {
+            float acc = 0.f;
+            for (int t = 0; t < L; ++t) {
+                acc += gam[t];
+                gam[t] = acc;
+                egam[t] = expf(acc);
+            }
+            for (int t = 0; t < L; ++t) fdec[t] = expf(acc - gam[t]);
+        }
+        __syncthreads();
+        // chain coefficients beta_t e^(gamma_t - gamma_s) (k_t . k_s): one warp per pair
+        if (!bad) {
+            for (int pr = warp; pr < L * (L - 1) / 2; pr += kT / 32) {
+                int t = 1, base = 0;
+                while (base + t <= pr) { base += t; ++t; }
+                const int s_ = pr - base;
+                float d = 0.f;
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = smem_desc(smem_u32(sm + OFF_TILE + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-                    const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS + (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, 2);
-                    mma_bf16(tmem, ad, bd, id, part > 0 || ks > 0);
+                for (int e = 0; e < 4; ++e) {
+                    const int m = lane * 4 + e;
+                    d = fmaf(bf16_at(sm + OFF_KEYS, sw128(t, m, kMaxPath)), bf16_at(sm + OFF_KEYS, sw128(s_, m, kMaxPath)), d);
                 }
-            mma_commit(&bar[1]);
-        }
-        ok = mbar_wait(&bar[1], 0) && ok;
-        tc_fence_after();
-        // chain solve for this row: u_t, then A[row][t] = e^(gamma_L - gamma_t) u_t
-        uint32_t wr[16];
-        tmem_ld16_nowait(tmem + lane_base, wr);
-        tmem_wait_ld();
-        float a[kMaxPath];
-#pragma unroll
-        for (int t = 0; t < kMaxPath; ++t) {
-            float u = 0.f;
-            if (t < L) {
-                u = bet[t] * (vp[t * kD + row] - egam[t] * __uint_as_float(wr[t]));
-#pragma unroll
-                for (int si = 0; si < t; ++si) u = fmaf(-coef[t * kMaxPath + si], a[si], u);
+                d = warp_sum(d);
+                if (lane == 0) coef[t * kMaxPath + s_] = bet[t] * expf(gam[t] - gam[s_]) * d;
             }
-            a[t] = u;
         }
+
+        // the state tile: row, columns 64 half .. 64 half + 63 into registers
+        ok = mbar_wait(&bar[0], ph_tile & 1) && ok;
+        ++ph_tile;
+        float s[64];
 #pragma unroll
-        for (int t = 0; t < kMaxPath; ++t) a[t] = t < L ? a[t] * fdec[t] : 0.f;
-        // A hi (half 0) or lo (half 1), core-matrix layout: 8 rows x 8 keys per 128 bytes
-        float part[kMaxPath];
-#pragma unroll
-        for (int t = 0; t < kMaxPath; ++t) {
-            const float h = __bfloat162float(__float2bfloat16_rn(a[t]));
-            part[t] = half == 0 ? h : a[t] - h;
+        for (int c = 0; c < 16; ++c) {
+            const float4 x = *reinterpret_cast<const float4 *>(tile + tile_index(row, half * 64 + c * 4));
+            s[c * 4 + 0] = x.x; s[c * 4 + 1] = x.y; s[c * 4 + 2] = x.z; s[c * 4 + 3] = x.w;
         }
-        uint8_t *abase = sm + OFF_A + half * 4096 + (row >> 3) * 256 + (row & 7) * 16;
+        __syncthreads();  // every thread holds its part; the tile space becomes S0 hi | lo
+        if (!bad) {
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
-            *reinterpret_cast<uint4 *>(abase + kh * 128) =
-                make_uint4(pack_bf16(part[kh * 8 + 0], part[kh * 8 + 1]), pack_bf16(part[kh * 8 + 2], part[kh * 8 + 3]),
-                           pack_bf16(part[kh * 8 + 4], part[kh * 8 + 5]), pack_bf16(part[kh * 8 + 6], part[kh * 8 + 7]));
+            for (int c = 0; c < 8; ++c) {
+                float hi[8], lw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    hi[e] = __bfloat162float(__float2bfloat16_rn(s[c * 8 + e]));
+                    lw[e] = s[c * 8 + e] - hi[e];
+                }
+                const uint32_t off = sw128(row, half * 64 + c * 8, kD);
+                *reinterpret_cast<uint4 *>(sm + OFF_TILE + off) =
+                    make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
+                *reinterpret_cast<uint4 *>(sm + OFF_TILE + 32768 + off) =
+                    make_uint4(pack_bf16(lw[0], lw[1]), pack_bf16(lw[2], lw[3]), pack_bf16(lw[4], lw[5]), pack_bf16(lw[6], lw[7]));
+            }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // U = A K (hi + lo) -> columns [128, 256); K is the same key tile read MN-major
-        if (tid == 0) {
+
+        if (!bad) {
+            // W = S0 K^T (hi + lo) -> tensor-memory columns [0, 16)
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16_f32(128, 16);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = smem_desc(smem_u32(sm + OFF_TILE + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
+                        const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS + (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, 2);
+                        mma_bf16(tmem, ad, bd, id, part > 0 || ks > 0);
+                    }
+                mma_commit(&bar[1]);
+            }
+            ok = mbar_wait(&bar[1], ph_mma & 1) && ok;
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 128) | (1u << 16);
-            const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS), 2048, 1024, 2);
-            mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A), 128, 256, 0), bd, id, false);
-            mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A + 4096), 128, 256, 0), bd, id, true);
-            mma_commit(&bar[2]);
-        }
-        ok = mbar_wait(&bar[2], 0) && ok;
-        tc_fence_after();
-        // S_new = e^gamma_L S0 + U, back into the tile in the TMA layout
-        const float eL = L > 0 ? egam[L - 1] : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            uint32_t ur[32];
-            tmem_ld32_nowait(tmem + lane_base + 128 + half * 64 + cc * 32, ur);
+            // chain solve for this row: u_t, then A[row][t] = e^(gamma_L - gamma_t) u_t
+            uint32_t wr[16];
+            tmem_ld16_nowait(tmem + lane_base, wr);
             tmem_wait_ld();
+            float a[kMaxPath];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int col = half * 64 + cc * 32 + c * 4;
-                float4 o;
-                o.x = fmaf(eL, s[cc * 32 + c * 4 + 0], __uint_as_float(ur[c * 4 + 0]));
-                o.y = fmaf(eL, s[cc * 32 + c * 4 + 1], __uint_as_float(ur[c * 4 + 1]));
-                o.z = fmaf(eL, s[cc * 32 + c * 4 + 2], __uint_as_float(ur[c * 4 + 2]));
-                o.w = fmaf(eL, s[cc * 32 + c * 4 + 3], __uint_as_float(ur[c * 4 + 3]));
-                *reinterpret_cast<float4 *>(tile + tile_index(row, col)) = o;
+            for (int t = 0; t < kMaxPath; ++t) {
+                float u = 0.f;
+                if (t < L) {
+                    u = bet[t] * (vp[t * kD + row] - egam[t] * __uint_as_float(wr[t]));
+#pragma unroll
+                    for (int si = 0; si < t; ++si) u = fmaf(-coef[t * kMaxPath + si], a[si], u);
+                }
+                a[t] = u;
+            }
+#pragma unroll
+            for (int t = 0; t < kMaxPath; ++t) a[t] = t < L ? a[t] * fdec[t] : 0.f;
+            // A hi (half 0) or lo (half 1), core-matrix layout: 8 rows x 8 keys per 128 bytes
+            float part[kMaxPath];
+#pragma unroll
+            for (int t = 0; t < kMaxPath; ++t) {
+                const float h = __bfloat162float(__float2bfloat16_rn(a[t]));
+                part[t] = half == 0 ? h : a[t] - h;
+            }
+            uint8_t *abase = sm + OFF_A + half * 4096 + (row >> 3) * 256 + (row & 7) * 16;
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh)
+                *reinterpret_cast<uint4 *>(abase + kh * 128) =
+                    make_uint4(pack_bf16(part[kh * 8 + 0], part[kh * 8 + 1]), pack_bf16(part[kh * 8 + 2], part[kh * 8 + 3]),
+                               pack_bf16(part[kh * 8 + 4], part[kh * 8 + 5]), pack_bf16(part[kh * 8 + 6], part[kh * 8 + 7]));
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            // U = A K (hi + lo) -> columns [128, 256); K is the same key tile read MN-major
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16_f32(128, 128) | (1u << 16);
+                const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS), 2048, 1024, 2);
+                mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A), 128, 256, 0), bd, id, false);
+                mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A + 4096), 128, 256, 0), bd, id, true);
+                mma_commit(&bar[2]);
+            }
+            ok = mbar_wait(&bar[2], ph_mma & 1) && ok;
+            ++ph_mma;
+            tc_fence_after();
+            // S_new = e^gamma_L S0 + U, back into the tile in the TMA layout
+            const float eL = L > 0 ? egam[L - 1] : 1.f;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t ur[32];
+                tmem_ld32_nowait(tmem + lane_base + 128 + half * 64 + cc * 32, ur);
+                tmem_wait_ld_into(ur);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int col = half * 64 + cc * 32 + c * 4;
+                    float4 o;
+                    o.x = fmaf(eL, s[cc * 32 + c * 4 + 0], __uint_as_float(ur[c * 4 + 0]));
+                    o.y = fmaf(eL, s[cc * 32 + c * 4 + 1], __uint_as_float(ur[c * 4 + 1]));
+                    o.z = fmaf(eL, s[cc * 32 + c * 4 + 2], __uint_as_float(ur[c * 4 + 2]));
+                    o.w = fmaf(eL, s[cc * 32 + c * 4 + 3], __uint_as_float(ur[c * 4 + 3]));
+                    *reinterpret_cast<float4 *>(tile + tile_index(row, col)) = o;
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            if (bad) {
+                flag(p.status, GDN_DEV_BAD_PATH);
+            } else {
+                for (int q = 0; q < 4; ++q) tma_store_2d(&tmSN, tile + q * kD * 32, q * 32, tile_row);
+                bulk_commit();
+                bulk_wait_read();  // the tile space is free for the next item's load
             }
         }
-        fence_proxy_async_smem();
+        ++it;
     }
+    if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        if (bad) {
-            flag(p.status, GDN_DEV_BAD_PATH);
-        } else {
-            for (int q = 0; q < 4; ++q) tma_store_2d(&tmSN, tile + q * kD * 32, q * 32, tile_row);
-            bulk_commit();
-            bulk_wait_read();
-        }
-        if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
-    }
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
@@ -330,13 +354,16 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream) {
     CUtensorMap tmS0, tmSN;
     if (!encode_state(&tmS0, a.S0, rows) || !encode_state(&tmSN, a.S_new, rows)) return cudaErrorInvalidValue;
     TcCommitParams p;
-    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.total = a.total_nodes;
+    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.total = a.total_nodes; p.items = a.batch * a.n_v_heads;
+    p.S0 = a.S0;
     p.offsets = a.node_offsets; p.parent = a.parent; p.poff = a.path_offsets; p.pidx = a.path_idx;
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
     cudaError_t e = cudaFuncSetAttribute(commit_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    commit_tc_kernel<<<(unsigned)a.batch * (unsigned)a.n_v_heads, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
+    // persistent: two blocks per SM
+    const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());
+    commit_tc_kernel<<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
     return cudaGetLastError();
 }
 

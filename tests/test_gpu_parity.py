@@ -505,3 +505,26 @@ def test_fast_commit_flags_long_and_bad_paths():
     torch.cuda.synchronize()
     assert int(status.item()) & 2
     assert torch.all(sentinel == 3.0)
+
+
+def test_fast_commit_many_items_with_a_bad_path():
+    # more items than resident blocks, mixed sizes and empty requests; one
+    # request's path is reversed (not root-first): it alone is flagged and skipped
+    tb = _tc_batch(23, _mixed_sizes(240))
+    lens = np.diff(tb.path_offsets)
+    bad = int(np.flatnonzero(lens >= 2)[3])
+    a, e = int(tb.path_offsets[bad]), int(tb.path_offsets[bad + 1])
+    tb.path_idx[a:e] = tb.path_idx[a:e][::-1].copy()
+    d = gb.upload(tb)
+    sentinel = torch.full_like(d["S0"], 3.0)
+    status = gb.new_status()
+    gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"],
+                       d["path_offsets"], d["path_idx"], tb.max_nodes, max_path=16, out=sentinel,
+                       dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+    assert torch.all(sentinel[bad] == 3.0)
+    ref, st = oracle.commit(tb)
+    assert st == 2
+    keep = [r for r in range(tb.batch) if r != bad]
+    assert rel_err(sentinel.cpu().numpy()[keep], ref[keep]) <= TOL_STATE
