@@ -411,6 +411,64 @@ def run_reference(args, rank, world):
     }
 
 
+def run_sweep(args):
+    """Fused verify against the per-branch baseline over the sweep grid: one JSON
+    line per (N, batch) point with both launch times (a CUDA graph of one launch,
+    replayed between CUDA events, L2 flushed before each replay)."""
+    import torch
+    from gated_delta_net_gb300 import binding as gb
+    from gated_delta_net_gb300 import build as gbuild
+
+    gbuild.build()
+    gb.lib()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_gbs, _, _ = load_peaks()
+    for n in (8, 16, 32, 64, 128, 256):
+        for batch in (1, 8, 32, 128):
+            tb = W.sweep_point(n, batch)
+            d = gb.upload(tb, device=dev)
+            status = gb.new_status(dev)
+            mask, depth = gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                                 dev_status=status)
+            times = {}
+            for impl, fn in (("fused", gb.gdn_tree_verify), ("branches", gb.gdn_tree_verify_branches)):
+                def launch(st):
+                    fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                       d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                       dev_status=status, stream=st)
+                # one eager launch (sets kernel attributes), then one launch captured
+                # in a CUDA graph, so that host-side launch cost stays out of the timing
+                launch(stream)
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    launch(torch.cuda.current_stream())
+                ms = []
+                for it in range(3 + args.sweep_reps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if it >= 3:
+                        ms.append(e0.elapsed_time(e1))
+                times[impl] = statistics.median(ms) * 1e3
+                del graph
+            gb.check_status(status)
+            vb = verify_bytes(tb)
+            print(json.dumps({
+                "kind": "sweep", "workload": tb.name, "n": n, "batch": batch,
+                "kernel": dominant_kernel(tb), "fused_us": times["fused"],
+                "branches_us": times["branches"], "speedup": times["branches"] / times["fused"],
+                "fused_node_tokens_per_s": tb.total_nodes / (times["fused"] * 1e-6),
+                "fused_hbm_frac": vb / (times["fused"] * 1e-6) / 1e9 / hbm_gbs}), flush=True)
+            del d, mask, depth
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,12 +480,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time fused verify against the per-branch baseline over the sweep grid")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:

@@ -204,7 +204,8 @@ cudaError_t launch_typed(const CommitParams &p, int batch, cudaStream_t stream) 
     const CommitSmem L = commit_layout(p.max_nodes, p.sw, DK);
     const size_t bytes = sizeof(float) * (size_t)L.floats + sizeof(int) * (size_t)L.ints;
     auto kern = commit_simt_kernel<Tin, DK>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    static int have[16];  // one per template instance
+    cudaError_t e = ensure_smem(kern, (int)bytes, have);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.dv / p.sw) * (unsigned)batch, p.hv_n);
     kern<<<grid, kThreads, bytes, stream>>>(p);

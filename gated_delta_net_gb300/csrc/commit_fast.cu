@@ -258,11 +258,13 @@ cudaError_t launch_commit_fast(const gdn_commit_args &a, cudaStream_t stream) {
     const dim3 grid((unsigned)a.batch * (unsigned)a.n_v_heads);
     cudaError_t e;
     if (a.qkv_dtype == GDN_BF16) {
-        e = cudaFuncSetAttribute(commit_fast_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        static int have[16];
+        e = ensure_smem(commit_fast_kernel<__nv_bfloat16>, (int)bytes, have);
         if (e != cudaSuccess) return e;
         commit_fast_kernel<__nv_bfloat16><<<grid, kT, bytes, stream>>>(tmS0, tmSN, p);
     } else {
-        e = cudaFuncSetAttribute(commit_fast_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        static int have[16];
+        e = ensure_smem(commit_fast_kernel<float>, (int)bytes, have);
         if (e != cudaSuccess) return e;
         commit_fast_kernel<float><<<grid, kT, bytes, stream>>>(tmS0, tmSN, p);
     }

@@ -359,7 +359,8 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream) {
     p.offsets = a.node_offsets; p.parent = a.parent; p.poff = a.path_offsets; p.pidx = a.path_idx;
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
-    cudaError_t e = cudaFuncSetAttribute(commit_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static int have[16];
+    cudaError_t e = ensure_smem(commit_tc_kernel, kSmemBytes, have);
     if (e != cudaSuccess) return e;
     // persistent: two blocks per SM
     const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());

@@ -57,6 +57,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // streaming multiprocessors on the current device (1 if the query fails)
 int sm_count();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device,
+// once per (kernel, device, size): `have` remembers the largest size set so far
+// per device.  Launches after the first make no attribute call, so they can be
+// captured into a CUDA graph.
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel kern, int bytes, int (&have)[16]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 16 && bytes <= have[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 16) have[dev] = bytes;
+    return e;
+}
+
 // tcgen05/TMA fast path; returns cudaErrorNotSupported when the shape is not covered
 bool verify_tc_supported(const gdn_verify_args &a);
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream);

@@ -220,7 +220,8 @@ cudaError_t launch_typed(const SimtParams &p, int batch, cudaStream_t stream) {
     const SmemLayout L = smem_layout(p.max_nodes, p.sw, DK);
     const size_t bytes = sizeof(float) * (size_t)L.floats + sizeof(int) * (size_t)L.ints;
     auto kern = verify_simt_kernel<Tin, Tout, DK>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    static int have[16];  // one per template instance
+    cudaError_t e = ensure_smem(kern, (int)bytes, have);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.dv / p.sw) * (unsigned)batch, p.hv_n);
     kern<<<grid, kThreads, bytes, stream>>>(p);

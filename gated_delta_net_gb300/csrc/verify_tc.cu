@@ -709,12 +709,13 @@ cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream) {
     const dim3 grid((unsigned)std::min(p.items, 2 * sm_count()));
     cudaError_t e;
     if (a.out_dtype == GDN_BF16) {
-        e = cudaFuncSetAttribute(verify_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        static int have[16];
+        e = ensure_smem(verify_tc_kernel<__nv_bfloat16>, kSmemBytes, have);
         if (e != cudaSuccess) return e;
         verify_tc_kernel<__nv_bfloat16><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, tmO, p);
     } else {
-        e = cudaFuncSetAttribute(verify_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        static int have[16];
+        e = ensure_smem(verify_tc_kernel<float>, kSmemBytes, have);
         if (e != cudaSuccess) return e;
         verify_tc_kernel<float><<<grid, kT, kSmemBytes, stream>>>(tmK, tmQ, tmV, tmO, p);
     }
