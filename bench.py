@@ -469,6 +469,90 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def run_helpers(args):
+    """The tree helpers on the throughput workload's shapes, one JSON line each:
+    topological relabel of the 64 trees under random labels (node-tokens/s) and
+    the row gathers that put the token rows into the new order (GB/s moved)."""
+    import torch
+    from gated_delta_net_gb300 import binding as gb
+    from gated_delta_net_gb300 import build as gbuild
+    from oracle import relabel as R
+
+    gbuild.build()
+    gb.lib()
+    dev = torch.device("cuda", 0)
+    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    rng = np.random.default_rng(5)
+    offs = tb.node_offsets.astype(np.int32)
+    shuffled = np.empty(tb.total_nodes, np.int32)
+    for b in range(tb.batch):
+        lo, hi = int(offs[b]), int(offs[b + 1])
+        perm = rng.permutation(hi - lo)
+        for i in range(hi - lo):
+            p = int(tb.parent[lo + i])
+            shuffled[lo + perm[i]] = -1 if p < 0 else perm[p]
+    d = gb.upload(tb, device=dev)
+    par_d = torch.from_numpy(shuffled).to(dev)
+    offs_d = d["node_offsets"]
+    status = gb.new_status(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    hbm_gbs, _, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(launch, reps=50):
+        launch(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            launch(torch.cuda.current_stream())
+        ms = []
+        for it in range(3 + reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 3:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms) * 1e-3
+
+    outs = {}
+
+    def relabel(st):
+        outs["r"] = gb.gdn_tree_relabel(par_d, offs_d, tb.max_nodes, dev_status=status, stream=st)
+
+    t_rel = timed(relabel)
+    order = outs["r"][0]
+    gb.check_status(status)
+    keys = ("q", "k", "v", "g", "beta")
+    bufs = {k: torch.empty_like(d[k]) for k in keys}
+
+    def gather(st):
+        for k in keys:
+            gb.gdn_gather_rows(d[k], order, offs_d, out=bufs[k], dev_status=status, stream=st)
+
+    t_g = timed(gather)
+    gb.check_status(status)
+    moved = 2 * sum(d[k].numel() * d[k].element_size() for k in keys)
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < 2.0:
+        R.relabel(shuffled, offs)
+        reps += 1
+    t_cpu = (time.perf_counter() - t0) / reps
+    rel_bytes = tb.total_nodes * 4 * 4 + 4 * (tb.batch + 1)
+    print(json.dumps({"kind": "helper", "op": "gdn_tree_relabel", "workload": tb.name + "_shuffled",
+                      "us": t_rel * 1e6, "node_tokens_per_s": tb.total_nodes / t_rel,
+                      "bytes": rel_bytes, "bound": "latency (one block per request, 8 pointer-jumping rounds)",
+                      "cpu_baseline": {"kind": "oracle", "value": tb.total_nodes / t_cpu,
+                                       "unit": "node-tokens/s", "cores": 1}}), flush=True)
+    print(json.dumps({"kind": "helper", "op": "gdn_gather_rows x5 (q, k, v, g, beta)",
+                      "workload": tb.name + "_shuffled", "us": t_g * 1e6, "bytes_moved": moved,
+                      "achieved_gbs": moved / t_g / 1e9, "hbm_frac": moved / t_g / 1e9 / hbm_gbs}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -483,6 +567,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time fused verify against the per-branch baseline over the sweep grid")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--helpers", action="store_true",
+                    help="time the tree relabel and row gather helpers on the throughput shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -491,6 +577,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.sweep:
         run_sweep(args)
+        return
+    if args.helpers:
+        run_helpers(args)
         return
     if args.impl == "reference":
         out = run_reference(args, rank, world)

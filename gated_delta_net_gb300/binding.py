@@ -78,6 +78,10 @@ def lib():
             fn.restype = ctypes.c_int
         L.gdn_tree_commit.argtypes = [ctypes.POINTER(CommitArgs), _P]
         L.gdn_tree_commit.restype = ctypes.c_int
+        L.gdn_tree_relabel.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]
+        L.gdn_tree_relabel.restype = ctypes.c_int
+        L.gdn_gather_rows.argtypes = [_P, _P, _P, _P, _I, _I, ctypes.c_int64, _P, _P]
+        L.gdn_gather_rows.restype = ctypes.c_int
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_tree_version.restype = ctypes.c_int
         _lib = L
@@ -149,6 +153,46 @@ def gdn_tree_build_desc(parent: torch.Tensor, node_offsets: torch.Tensor, max_no
                                      int(max_nodes), _ptr(anc_mask), words, _ptr(depth),
                                      _ptr(dev_status), _stream(stream)))
     return anc_mask, depth
+
+
+def gdn_tree_relabel(parent: torch.Tensor, node_offsets: torch.Tensor, max_nodes: int,
+                     dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Topological relabelling by (depth, old id): (order, rank, parent_out), each [T] int32
+    with request-local ids."""
+    _dev(parent, "parent", torch.int32)
+    _dev(node_offsets, "node_offsets", torch.int32)
+    T = parent.numel()
+    order = torch.empty(T, dtype=torch.int32, device=parent.device)
+    rank = torch.empty_like(order)
+    parent_out = torch.empty_like(order)
+    _check(lib().gdn_tree_relabel(_ptr(parent), _ptr(node_offsets), node_offsets.numel() - 1, T,
+                                  int(max_nodes), _ptr(order), _ptr(rank), _ptr(parent_out),
+                                  _ptr(dev_status), _stream(stream)))
+    return order, rank, parent_out
+
+
+def gdn_gather_rows(src: torch.Tensor, index: torch.Tensor, node_offsets: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """Rows permuted within each request: out[lo + j] = src[lo + index[lo + j]]."""
+    _dev(src, "src")
+    _dev(index, "index", torch.int32)
+    _dev(node_offsets, "node_offsets", torch.int32)
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    T = src.shape[0]
+    if index.numel() != T:
+        raise ValueError("index must have one entry per row")
+    if out is None:
+        out = torch.empty_like(src)
+    _dev(out, "out", src.dtype)
+    if out.shape != src.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like src")
+    row_bytes = src[0].numel() * src.element_size() if T else 16
+    _check(lib().gdn_gather_rows(_ptr(src), _ptr(out), _ptr(index), _ptr(node_offsets),
+                                 node_offsets.numel() - 1, T, row_bytes, _ptr(dev_status),
+                                 _stream(stream)))
+    return out
 
 
 def _verify_args(q, k, v, g, beta, S0, node_offsets, parent, anc_mask, depth, max_nodes,

@@ -112,6 +112,43 @@ int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offsets, int3
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "build_desc launch");
 }
 
+int gdn_tree_relabel(const int32_t *parent_in, const int32_t *node_offsets, int32_t batch, int32_t total_nodes,
+                     int32_t max_nodes, int32_t *order, int32_t *rank, int32_t *parent_out, int32_t *dev_status,
+                     void *stream) {
+    g_err[0] = 0;
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", total_nodes);
+    if (max_nodes < 1) return fail(GDN_ERR_INVALID_ARG, "max_nodes %d < 1", max_nodes);
+    if (max_nodes > gdn::kMaxNodes)
+        return fail(GDN_ERR_UNSUPPORTED, "max_nodes %d > %d", max_nodes, gdn::kMaxNodes);
+    if (batch == 0 || total_nodes == 0) return GDN_OK;
+    if (!parent_in || !node_offsets || !order || !rank || !parent_out)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    cudaError_t e = gdn::launch_relabel(parent_in, node_offsets, batch, total_nodes, max_nodes, order, rank,
+                                        parent_out, dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "relabel launch");
+}
+
+int gdn_gather_rows(const void *src, void *dst, const int32_t *index, const int32_t *node_offsets, int32_t batch,
+                    int32_t total_nodes, int64_t row_bytes, int32_t *dev_status, void *stream) {
+    g_err[0] = 0;
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", total_nodes);
+    if (batch > 65535) return fail(GDN_ERR_UNSUPPORTED, "batch %d > 65535", batch);
+    if (row_bytes <= 0 || row_bytes % 16)
+        return fail(GDN_ERR_INVALID_ARG, "row_bytes %lld must be a positive multiple of 16", (long long)row_bytes);
+    if (batch == 0 || total_nodes == 0) return GDN_OK;
+    if (!src || !dst || !index || !node_offsets) return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15)
+        return fail(GDN_ERR_INVALID_ARG, "src and dst must be 16-byte aligned");
+    const char *s = static_cast<const char *>(src), *d = static_cast<const char *>(dst);
+    const int64_t span = (int64_t)total_nodes * row_bytes;
+    if (s < d + span && d < s + span) return fail(GDN_ERR_INVALID_ARG, "dst overlaps src");
+    cudaError_t e = gdn::launch_gather_rows(src, dst, index, node_offsets, batch, total_nodes, row_bytes,
+                                            dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gather launch");
+}
+
 int gdn_tree_verify(const gdn_verify_args *a, void *stream) {
     g_err[0] = 0;
     int st = check_verify(a);

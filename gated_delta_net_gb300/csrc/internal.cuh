@@ -40,6 +40,11 @@ cudaError_t launch_build_desc(const int32_t *parent, const int32_t *node_offsets
                               int32_t *depth, int32_t *dev_status, cudaStream_t stream);
 
 cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream);
+cudaError_t launch_relabel(const int32_t *parent_in, const int32_t *node_offsets, int batch, int total,
+                           int max_nodes, int32_t *order, int32_t *rank, int32_t *parent_out,
+                           int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_gather_rows(const void *src, void *dst, const int32_t *index, const int32_t *node_offsets,
+                               int batch, int total, int64_t row_bytes, int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_verify_branches(const gdn_verify_args &a, cudaStream_t stream);
 cudaError_t launch_commit_simt(const gdn_commit_args &a, cudaStream_t stream);
 

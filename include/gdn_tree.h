@@ -98,6 +98,40 @@ GDN_API int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offse
                         int32_t max_nodes, uint32_t *anc_mask, int32_t mask_words,
                         int32_t *depth, int32_t *dev_status, void *stream);
 
+/*
+ * gdn_tree_relabel -- topological order for a tree given in any order (same
+ * section, Solution bullet 1: the tree is processed parent before child).
+ * Per request, nodes are sorted by (depth, old id), which is unique:
+ *   parent_in  [T] int32: request-local parent ids in any labelling (-1 = root;
+ *              forests allowed).
+ *   order      [T] int32: order[lo + j] = old id of the node placed j-th.
+ *   rank       [T] int32: rank[lo + i] = new id of old node i.
+ *   parent_out [T] int32: parents in new ids; parent_out[lo + j] < j.
+ * Integer work, bit-exact.  total_nodes = T.  A request whose parents do not
+ * form a forest (a parent outside [-1, n), a self-parent, a cycle) sets
+ * GDN_DEV_BAD_TREE and its rows of the three outputs are left untouched.
+ * max_nodes <= 256.  Token rows are then gathered by `order` (e.g. with
+ * gdn_gather_rows) before gdn_tree_build_desc.
+ */
+GDN_API int gdn_tree_relabel(const int32_t *parent_in, const int32_t *node_offsets, int32_t batch,
+                             int32_t total_nodes, int32_t max_nodes, int32_t *order, int32_t *rank,
+                             int32_t *parent_out, int32_t *dev_status, void *stream);
+
+/*
+ * gdn_gather_rows -- permute rows within each request: dst row lo + j = src
+ * row lo + index[lo + j], index request-local (no counterpart in the pages: the
+ * data movement that goes with gdn_tree_relabel).  With index = order it puts
+ * token rows (q, k, v, g, beta) into the new order; with index = rank it maps
+ * outputs in the new order back to the old labels.
+ *   src, dst  [T] rows of row_bytes bytes each (row_bytes > 0, a multiple of
+ *             16; both pointers 16-byte aligned; dst must not overlap src).
+ * An index outside [0, n) sets GDN_DEV_BAD_DESC and leaves that dst row
+ * untouched.  batch <= 65535.
+ */
+GDN_API int gdn_gather_rows(const void *src, void *dst, const int32_t *index, const int32_t *node_offsets,
+                            int32_t batch, int32_t total_nodes, int64_t row_bytes, int32_t *dev_status,
+                            void *stream);
+
 typedef struct {
     int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
     int32_t total_nodes;   /* T = node_offsets[batch]: rows of q, k, v, g, beta, o */

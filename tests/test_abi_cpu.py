@@ -24,9 +24,9 @@ def declared_symbols():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_symbols() == sorted(["gdn_last_error", "gdn_tree_build_desc", "gdn_tree_commit",
-                                         "gdn_tree_verify", "gdn_tree_verify_branches",
-                                         "gdn_tree_version"])
+    assert declared_symbols() == sorted(["gdn_gather_rows", "gdn_last_error", "gdn_tree_build_desc",
+                                         "gdn_tree_commit", "gdn_tree_relabel", "gdn_tree_verify",
+                                         "gdn_tree_verify_branches", "gdn_tree_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -98,6 +98,28 @@ def test_build_desc_rejects_bad_arguments(L):
     assert f(fake, fake, 1, 100, fake, 2, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
     assert f(None, fake, 1, 12, fake, 1, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
     assert f(None, None, 0, 12, None, 1, None, None, None) == binding.GDN_OK
+
+
+def test_relabel_rejects_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    f = L.gdn_tree_relabel
+    assert f(fake, fake, -1, 4, 12, fake, fake, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(fake, fake, 1, -1, 12, fake, fake, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(fake, fake, 1, 4, 0, fake, fake, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(fake, fake, 1, 4, 300, fake, fake, fake, fake, None) == binding.GDN_ERR_UNSUPPORTED
+    assert f(fake, fake, 1, 4, 12, None, fake, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(None, None, 0, 0, 12, None, None, None, None, None) == binding.GDN_OK
+
+
+def test_gather_rejects_bad_arguments(L):
+    a, b = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x100000)
+    f = L.gdn_gather_rows
+    assert f(a, b, a, a, 1, 4, 24, None, None) == binding.GDN_ERR_INVALID_ARG      # not a multiple of 16
+    assert f(a, b, a, a, 1, 4, 0, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(a, ctypes.c_void_p(0x1008), a, a, 1, 4, 32, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(a, ctypes.c_void_p(0x1010), a, a, 1, 4, 32, None, None) == binding.GDN_ERR_INVALID_ARG  # overlap
+    assert f(None, b, a, a, 1, 4, 32, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert f(None, None, None, None, 0, 0, 32, None, None) == binding.GDN_OK
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
