@@ -547,6 +547,32 @@ def run_helpers(args):
                       "bytes": rel_bytes, "bound": "latency (one block per request, 8 pointer-jumping rounds)",
                       "cpu_baseline": {"kind": "oracle", "value": tb.total_nodes / t_cpu,
                                        "unit": "node-tokens/s", "cores": 1}}), flush=True)
+    # states at four candidate leaves per request (the accepted one and three more)
+    leaves = []
+    for b in range(tb.batch):
+        lo, hi = int(offs[b]), int(offs[b + 1])
+        par = tb.parent[lo:hi]
+        has_child = np.zeros(hi - lo, bool)
+        has_child[par[par >= 0]] = True
+        cand = [int(tb.path_idx[tb.path_offsets[b + 1] - 1])]
+        cand += [int(i) for i in np.flatnonzero(~has_child) if int(i) != cand[0]][:3]
+        leaves += [(b, i) for i in cand]
+    sel_req = torch.tensor([b for b, _ in leaves], dtype=torch.int32, device=dev)
+    sel_node = torch.tensor([i for _, i in leaves], dtype=torch.int32, device=dev)
+    mask, _ = gb.gdn_tree_build_desc(d["parent"], offs_d, tb.max_nodes, dev_status=status)
+    S_sel = torch.empty((len(leaves), tb.n_v_heads, tb.d_v, tb.d_k), dtype=torch.float32, device=dev)
+
+    def states(st):
+        gb.gdn_tree_states(d["k"], d["v"], d["g"], d["beta"], d["S0"], offs_d, d["parent"], mask,
+                           sel_req, sel_node, tb.max_nodes, out=S_sel, dev_status=status, stream=st)
+
+    t_s = timed(states, reps=20)
+    gb.check_status(status)
+    st_bytes = len(leaves) * tb.n_v_heads * tb.d_v * tb.d_k * 4 * 2
+    print(json.dumps({"kind": "helper", "op": "gdn_tree_states (4 leaves per request)",
+                      "workload": tb.name, "selections": len(leaves), "us": t_s * 1e6,
+                      "state_bytes": st_bytes, "achieved_gbs": st_bytes / t_s / 1e9,
+                      "hbm_frac": st_bytes / t_s / 1e9 / hbm_gbs}), flush=True)
     print(json.dumps({"kind": "helper", "op": "gdn_gather_rows x5 (q, k, v, g, beta)",
                       "workload": tb.name + "_shuffled", "us": t_g * 1e6, "bytes_moved": moved,
                       "achieved_gbs": moved / t_g / 1e9, "hbm_frac": moved / t_g / 1e9 / hbm_gbs}),

@@ -43,6 +43,14 @@ class CommitArgs(ctypes.Structure):
                 ("path_idx", _P), ("S_new", _P), ("dev_status", _P)]
 
 
+class StatesArgs(ctypes.Structure):
+    _fields_ = [("batch", _I), ("n_k_heads", _I), ("n_v_heads", _I), ("d_k", _I), ("d_v", _I),
+                ("total_nodes", _I), ("max_nodes", _I), ("qkv_dtype", _I),
+                ("node_offsets", _P), ("k", _P), ("v", _P), ("g", _P), ("beta", _P), ("S0", _P),
+                ("parent", _P), ("anc_mask", _P), ("mask_words", _I), ("n_sel", _I),
+                ("sel_request", _P), ("sel_node", _P), ("S_sel", _P), ("dev_status", _P)]
+
+
 class GdnError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"gdn status {code}: {msg}")
@@ -78,6 +86,8 @@ def lib():
             fn.restype = ctypes.c_int
         L.gdn_tree_commit.argtypes = [ctypes.POINTER(CommitArgs), _P]
         L.gdn_tree_commit.restype = ctypes.c_int
+        L.gdn_tree_states.argtypes = [ctypes.POINTER(StatesArgs), _P]
+        L.gdn_tree_states.restype = ctypes.c_int
         L.gdn_tree_relabel.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]
         L.gdn_tree_relabel.restype = ctypes.c_int
         L.gdn_gather_rows.argtypes = [_P, _P, _P, _P, _I, _I, ctypes.c_int64, _P, _P]
@@ -153,6 +163,35 @@ def gdn_tree_build_desc(parent: torch.Tensor, node_offsets: torch.Tensor, max_no
                                      int(max_nodes), _ptr(anc_mask), words, _ptr(depth),
                                      _ptr(dev_status), _stream(stream)))
     return anc_mask, depth
+
+
+def gdn_tree_states(k, v, g, beta, S0, node_offsets, parent, anc_mask, sel_request, sel_node,
+                    max_nodes: int, out=None, dev_status=None, stream=None) -> torch.Tensor:
+    """The state at each selected node [n_sel, Hv, d_v, d_k] (fp32)."""
+    for name, t in (("k", k), ("v", v)):
+        _dev(t, name)
+    for name, t in (("g", g), ("beta", beta), ("S0", S0)):
+        _dev(t, name, torch.float32)
+    for name, t in (("node_offsets", node_offsets), ("parent", parent), ("anc_mask", anc_mask),
+                    ("sel_request", sel_request), ("sel_node", sel_node)):
+        _dev(t, name, torch.int32)
+    T, Hk, dk = k.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    B = node_offsets.numel() - 1
+    n_sel = sel_request.numel()
+    if sel_node.numel() != n_sel or S0.shape != (B, Hv, dv, dk):
+        raise ValueError("inconsistent selection / S0 shapes")
+    if out is None:
+        out = torch.empty((n_sel, Hv, dv, dk), dtype=torch.float32, device=S0.device)
+    _dev(out, "out", torch.float32)
+    if out.shape != (n_sel, Hv, dv, dk):
+        raise ValueError("out must be [n_sel, Hv, d_v, d_k]")
+    a = StatesArgs(B, Hk, Hv, dk, dv, T, int(max_nodes), _code(k.dtype), _ptr(node_offsets), _ptr(k),
+                   _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(parent), _ptr(anc_mask),
+                   anc_mask.shape[1] if anc_mask.dim() == 2 else 1, n_sel, _ptr(sel_request),
+                   _ptr(sel_node), _ptr(out), _ptr(dev_status))
+    _check(lib().gdn_tree_states(ctypes.byref(a), _stream(stream)))
+    return out
 
 
 def gdn_tree_relabel(parent: torch.Tensor, node_offsets: torch.Tensor, max_nodes: int,

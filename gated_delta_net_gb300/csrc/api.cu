@@ -185,4 +185,25 @@ int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
 }
 
+int gdn_tree_states(const gdn_states_args *a, void *stream) {
+    g_err[0] = 0;
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
+    int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
+    if (st) return st;
+    if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
+    if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
+    if (a->n_sel < 0) return fail(GDN_ERR_INVALID_ARG, "n_sel %d < 0", a->n_sel);
+    if (a->batch == 0 || a->n_sel == 0) return GDN_OK;
+    if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent || !a->anc_mask ||
+        !a->sel_request || !a->sel_node || !a->S_sel)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (a->mask_words < (a->max_nodes + 31) / 32 || a->mask_words > gdn::kMaxWords)
+        return fail(GDN_ERR_INVALID_ARG, "mask_words %d must be in [%d, %d]", a->mask_words,
+                    (a->max_nodes + 31) / 32, gdn::kMaxWords);
+    if (!gdn::states_tc_supported(*a))
+        return fail(GDN_ERR_UNSUPPORTED, "states: bf16 k/v with d_k = d_v = 128 and 16-byte aligned tensors only");
+    cudaError_t e = gdn::launch_states_tc(*a, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "states launch");
+}
+
 }  // extern "C"

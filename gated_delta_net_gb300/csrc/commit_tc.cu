@@ -8,6 +8,10 @@
 //     S_new = e^gamma_L S0 + sum_t e^(gamma_L - gamma_t) u_t k_t^T
 // which equals running the gated delta rule along the path.
 //
+// The same kernel, instantiated for selected nodes, gives the state at any
+// chosen node (the path is the node's ancestor-mask row, root first), so that
+// a later commit of one of them needs no recompute.
+//
 // Persistent blocks (two per SM) walk the (request, value head) items; the next
 // item's state tile is requested into L2 while the current one is committed.
 // Both contractions are GEMMs with a 16-wide side and run on tcgen05 with fp32
@@ -46,9 +50,11 @@ constexpr int OFF_BAR = OFF_MISC + 16;
 constexpr int kSmemBytes = OFF_BAR + 3 * 8;
 
 struct TcCommitParams {
-    int hk_n, hv_n, total, items;
+    int hk_n, hv_n, total, items, batch, words;
     const float *S0;
     const int32_t *offsets, *parent, *poff, *pidx;
+    const int32_t *sel_req, *sel_node;  // selected nodes (state mode)
+    const uint32_t *mask;               // ancestor-mask rows (state mode)
     const __nv_bfloat16 *k, *v;
     const float *g, *beta;
     int32_t *status;
@@ -74,6 +80,26 @@ __device__ __forceinline__ float bf16_at(const uint8_t *base, uint32_t off) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
 }
 
+// The t-th set bit (0-based, ascending) of a multi-word mask row, or -1.
+__device__ __forceinline__ int nth_bit(const uint32_t (&m)[kMaxWords], int words, int t) {
+#pragma unroll
+    for (int w = 0; w < kMaxWords; ++w) {
+        if (w >= words) break;
+        const int c = __popc(m[w]);
+        if (t < c) {
+            uint32_t x = m[w];
+            for (int k = 0; k < t; ++k) x &= x - 1;
+            return w * 32 + __ffs(x) - 1;
+        }
+        t -= c;
+    }
+    return -1;
+}
+
+// kSel = false: item (request, value head) commits the request's accepted path
+// into S_new.  kSel = true: item (selection s, value head) writes the state at
+// node sel_node[s] of request sel_req[s] into row block s of S_sel.
+template <bool kSel>
 __global__ void __launch_bounds__(kT, 2)
 commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmSN,
                  TcCommitParams p) {
@@ -115,30 +141,69 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     int it = 0;                        // items committed by this block
 
     for (int idx = blockIdx.x; idx < p.items; idx += gridDim.x) {
-        const int hv = idx % p.hv_n, b = idx / p.hv_n;
+        const int hv = idx % p.hv_n, grp = idx / p.hv_n;
         const int hk = hv / (p.hv_n / p.hk_n);
-        const int lo = p.offsets[b];
-        const int n = p.offsets[b + 1] - lo;
-        const int pa = p.poff[b];
-        const int L = p.poff[b + 1] - pa;
-        const int tile_row = idx * kD;
-        if (L < 0 || L > kMaxPath || L > n || lo < 0 || lo + n > p.total) {
-            if (tid == 0) flag(p.status, L > kMaxPath && L <= n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
+        const int b = kSel ? __ldg(p.sel_req + grp) : grp;
+        if (kSel && (b < 0 || b >= p.batch)) {
+            if (tid == 0) flag(p.status, GDN_DEV_BAD_PATH);
             continue;
         }
+        const int lo = p.offsets[b];
+        const int n = p.offsets[b + 1] - lo;
+        int L, pa = 0, sel = -1;
+        uint32_t mrow[kMaxWords];
+        if constexpr (kSel) {
+            // the selected node's path: the set bits of its ancestor-mask row
+            sel = __ldg(p.sel_node + grp);
+            if (sel < 0 || sel >= n || lo < 0 || lo + n > p.total) {
+                if (tid == 0) flag(p.status, GDN_DEV_BAD_PATH);
+                continue;
+            }
+            L = 0;
+#pragma unroll
+            for (int w = 0; w < kMaxWords; ++w) {
+                mrow[w] = w < p.words ? __ldg(p.mask + (int64_t)(lo + sel) * p.words + w) : 0u;
+                L += __popc(mrow[w]);
+            }
+            if (L > kMaxPath) {
+                if (tid == 0) flag(p.status, GDN_DEV_TOO_DEEP);
+                continue;
+            }
+        } else {
+            pa = p.poff[b];
+            L = p.poff[b + 1] - pa;
+            if (L < 0 || L > kMaxPath || L > n || lo < 0 || lo + n > p.total) {
+                if (tid == 0) flag(p.status, L > kMaxPath && L <= n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
+                continue;
+            }
+        }
+        const int row_in = (b * p.hv_n + hv) * kD, tile_row = idx * kD;
         int *bad_flag = s_bad + (it & 1);
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar[0], kD * kD * 4);
-            for (int q = 0; q < 4; ++q) tma_load_2d(tile + q * kD * 32, &tmS0, &bar[0], q * 32, tile_row);
-            if (idx + (int)gridDim.x < p.items)  // the next item's state tile, into L2
-                prefetch_l2(p.S0 + (int64_t)(idx + gridDim.x) * (kD * kD), kD * kD * 4);
+            for (int q = 0; q < 4; ++q) tma_load_2d(tile + q * kD * 32, &tmS0, &bar[0], q * 32, row_in);
+            const int nx = idx + (int)gridDim.x;  // the next item's state tile, into L2
+            if (nx < p.items) {
+                const int nb = kSel ? __ldg(p.sel_req + nx / p.hv_n) : nx / p.hv_n;
+                if (nb >= 0 && nb < p.batch)
+                    prefetch_l2(p.S0 + ((int64_t)nb * p.hv_n + nx % p.hv_n) * (kD * kD), kD * kD * 4);
+            }
         }
-        // path validation
+        // path validation: root first, parent -> child edges (and, for a selected
+        // node, a path that ends at that node)
+        if (kSel && L == 0 && tid == 0) atomicOr(bad_flag, 1);
         if (tid < L) {
-            const int node = p.pidx[pa + tid];
-            const int expect = tid == 0 ? -1 : p.pidx[pa + tid - 1];
+            int node, expect;
+            if constexpr (kSel) {
+                node = nth_bit(mrow, p.words, tid);
+                expect = tid == 0 ? -1 : nth_bit(mrow, p.words, tid - 1);
+            } else {
+                node = p.pidx[pa + tid];
+                expect = tid == 0 ? -1 : p.pidx[pa + tid - 1];
+            }
             pn[tid] = node;
-            if (node < 0 || node >= n || p.parent[lo + node] != expect) atomicOr(bad_flag, 1);
+            if (node < 0 || node >= n || p.parent[lo + node] != expect || (kSel && tid == L - 1 && node != sel))
+                atomicOr(bad_flag, 1);
         }
         __syncthreads();
         const bool bad = *bad_flag != 0;
@@ -311,7 +376,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
         __syncthreads();
         if (tid == 0) {
             if (bad) {
-                flag(p.status, GDN_DEV_BAD_PATH);
+                flag(p.status, kSel ? GDN_DEV_BAD_DESC : GDN_DEV_BAD_PATH);
             } else {
                 for (int q = 0; q < 4; ++q) tma_store_2d(&tmSN, tile + q * kD * 32, q * 32, tile_row);
                 bulk_commit();
@@ -353,18 +418,44 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream) {
     const int64_t rows = (int64_t)a.batch * a.n_v_heads * kD;
     CUtensorMap tmS0, tmSN;
     if (!encode_state(&tmS0, a.S0, rows) || !encode_state(&tmSN, a.S_new, rows)) return cudaErrorInvalidValue;
-    TcCommitParams p;
+    TcCommitParams p = {};
     p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.total = a.total_nodes; p.items = a.batch * a.n_v_heads;
-    p.S0 = a.S0;
+    p.batch = a.batch; p.S0 = a.S0;
     p.offsets = a.node_offsets; p.parent = a.parent; p.poff = a.path_offsets; p.pidx = a.path_idx;
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
     static int have[16];
-    cudaError_t e = ensure_smem(commit_tc_kernel, kSmemBytes, have);
+    cudaError_t e = ensure_smem(commit_tc_kernel<false>, kSmemBytes, have);
     if (e != cudaSuccess) return e;
     // persistent: two blocks per SM
     const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());
-    commit_tc_kernel<<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
+    commit_tc_kernel<false><<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
+    return cudaGetLastError();
+}
+
+bool states_tc_supported(const gdn_states_args &a) {
+    return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && aligned16(a.S0) && aligned16(a.S_sel) &&
+           aligned16(a.k) && aligned16(a.v) && (int64_t)a.batch * a.n_v_heads * kD <= 2147483647LL &&
+           (int64_t)a.n_sel * a.n_v_heads * kD <= 2147483647LL && tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_states_tc(const gdn_states_args &a, cudaStream_t stream) {
+    CUtensorMap tmS0, tmSN;
+    if (!encode_state(&tmS0, a.S0, (int64_t)a.batch * a.n_v_heads * kD) ||
+        !encode_state(&tmSN, a.S_sel, (int64_t)a.n_sel * a.n_v_heads * kD))
+        return cudaErrorInvalidValue;
+    TcCommitParams p = {};
+    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.total = a.total_nodes; p.items = a.n_sel * a.n_v_heads;
+    p.batch = a.batch; p.words = a.mask_words; p.S0 = a.S0;
+    p.offsets = a.node_offsets; p.parent = a.parent; p.sel_req = a.sel_request; p.sel_node = a.sel_node;
+    p.mask = a.anc_mask;
+    p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
+    p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
+    static int have[16];
+    cudaError_t e = ensure_smem(commit_tc_kernel<true>, kSmemBytes, have);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());
+    commit_tc_kernel<true><<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
     return cudaGetLastError();
 }
 

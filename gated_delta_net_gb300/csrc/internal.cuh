@@ -56,6 +56,10 @@ cudaError_t launch_commit_fast(const gdn_commit_args &a, cudaStream_t stream);
 bool commit_tc_supported(const gdn_commit_args &a);
 cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream);
 
+// the same kernel writing the states at selected nodes
+bool states_tc_supported(const gdn_states_args &a);
+cudaError_t launch_states_tc(const gdn_states_args &a, cudaStream_t stream);
+
 // driver entry point for TMA descriptors (nullptr when the driver lacks it)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

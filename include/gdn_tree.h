@@ -209,6 +209,39 @@ typedef struct {
  */
 GDN_API int gdn_tree_commit(const gdn_commit_args *args, void *stream);
 
+typedef struct {
+    int32_t batch, n_k_heads, n_v_heads, d_k, d_v;
+    int32_t total_nodes;   /* T = node_offsets[batch]: rows of k, v, g, beta */
+    int32_t max_nodes;     /* upper bound on any request's node count (<= 256) */
+    int32_t qkv_dtype;     /* gdn_dtype of k, v */
+    const int32_t *node_offsets;
+    const void *k, *v;
+    const float *g, *beta, *S0;
+    const int32_t *parent;
+    const uint32_t *anc_mask;     /* from gdn_tree_build_desc */
+    int32_t mask_words;
+    int32_t n_sel;                /* number of selected nodes */
+    const int32_t *sel_request;   /* [n_sel] request of each selected node */
+    const int32_t *sel_node;      /* [n_sel] request-local node id */
+    float *S_sel;                 /* [n_sel][Hv][d_v][d_k]: the state at each selected node */
+    int32_t *dev_status;
+} gdn_states_args;
+
+/*
+ * gdn_tree_states -- the state S_i at chosen nodes i: the commit of i's own
+ * root-to-node path (same section, Solution bullet 4, applied to a node that
+ * is not yet accepted), so that committing one of them later needs no
+ * recompute (the scope table's per-node-state variant; the pages have no
+ * counterpart beyond the commit itself).  A node's path is read from its
+ * anc_mask row (root first) and checked against parent[]; a row that does not
+ * follow parent -> child edges to the node sets GDN_DEV_BAD_DESC, a selection
+ * outside its request sets GDN_DEV_BAD_PATH, a path longer than 16 sets
+ * GDN_DEV_TOO_DEEP, and that selection's S_sel block is left unwritten.
+ * Supported: bf16 k/v with d_k = d_v = 128 (else GDN_ERR_UNSUPPORTED); fp32
+ * accumulation throughout, same numerics as gdn_tree_commit's fast path.
+ */
+GDN_API int gdn_tree_states(const gdn_states_args *args, void *stream);
+
 /* Message for the last non-OK return on this thread ("" if none). */
 GDN_API const char *gdn_last_error(void);
 

@@ -25,8 +25,9 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gdn_gather_rows", "gdn_last_error", "gdn_tree_build_desc",
-                                         "gdn_tree_commit", "gdn_tree_relabel", "gdn_tree_verify",
-                                         "gdn_tree_verify_branches", "gdn_tree_version"])
+                                         "gdn_tree_commit", "gdn_tree_relabel", "gdn_tree_states",
+                                         "gdn_tree_verify", "gdn_tree_verify_branches",
+                                         "gdn_tree_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -98,6 +99,31 @@ def test_build_desc_rejects_bad_arguments(L):
     assert f(fake, fake, 1, 100, fake, 2, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
     assert f(None, fake, 1, 12, fake, 1, fake, fake, None) == binding.GDN_ERR_INVALID_ARG
     assert f(None, None, 0, 12, None, 1, None, None, None) == binding.GDN_OK
+
+
+def _states_args(**kw):
+    fake = 0x1000
+    a = dict(batch=1, n_k_heads=1, n_v_heads=2, d_k=128, d_v=128, total_nodes=4, max_nodes=4,
+             qkv_dtype=binding.GDN_BF16, node_offsets=fake, k=fake, v=fake, g=fake, beta=fake,
+             S0=fake, parent=fake, anc_mask=fake, mask_words=1, n_sel=2, sel_request=fake,
+             sel_node=fake, S_sel=fake, dev_status=None)
+    a.update(kw)
+    return binding.StatesArgs(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_sel=-1), binding.GDN_ERR_INVALID_ARG),
+    (dict(sel_node=None), binding.GDN_ERR_INVALID_ARG),
+    (dict(mask_words=0), binding.GDN_ERR_INVALID_ARG),
+    (dict(d_k=64, d_v=64), binding.GDN_ERR_UNSUPPORTED),
+    (dict(qkv_dtype=binding.GDN_F32), binding.GDN_ERR_UNSUPPORTED),
+    (dict(n_v_heads=3, n_k_heads=2), binding.GDN_ERR_INVALID_ARG),
+    (dict(n_sel=0, S_sel=None), binding.GDN_OK),
+])
+def test_states_rejects_bad_arguments(L, kw, code):
+    a = _states_args(**kw)
+    assert L.gdn_tree_states(ctypes.byref(a), None) == code
+    assert L.gdn_tree_states(None, None) == binding.GDN_ERR_INVALID_ARG
 
 
 def test_relabel_rejects_bad_arguments(L):
