@@ -323,3 +323,14 @@ def custom(seed: int, parents: Sequence[np.ndarray], n_k_heads: int = 1, n_v_hea
            d: int = 16, qkv_dtype: str = "f32", path_fn=path_random_leaf) -> TreeBatch:
     """Arbitrary shapes for edge-case tests."""
     return make_batch("custom", seed, parents, n_k_heads, n_v_heads, d, d, qkv_dtype, path_fn)
+
+
+def grow_draws(seed: int, node_offsets: np.ndarray, max_children: int = 8):
+    """Random inputs of the top-w tree construction, indexed by node row:
+    children counts c ~ Geometric(1/2) clipped to [1, max_children] (mean about 2)
+    and Exp(1) score decrements e [T][max_children], float32."""
+    rng = np.random.default_rng(seed)
+    T = int(node_offsets[-1])
+    c = np.minimum(rng.geometric(0.5, T), max_children).astype(np.int32)
+    e = rng.exponential(1.0, (T, max_children)).astype(np.float32)
+    return c, e
