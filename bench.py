@@ -573,6 +573,25 @@ def run_helpers(args):
                       "workload": tb.name, "selections": len(leaves), "us": t_s * 1e6,
                       "state_bytes": st_bytes, "achieved_gbs": st_bytes / t_s / 1e9,
                       "hbm_frac": st_bytes / t_s / 1e9 / hbm_gbs}), flush=True)
+    # top-w best-first construction of the 64 trees of 128 nodes, w = 1 and w = 8
+    from oracle import grow as G
+    c_np, e_np = W.grow_draws(7, offs)
+    c_d, e_d = torch.from_numpy(c_np).to(dev), torch.from_numpy(e_np).to(dev)
+    for width in (1, 8):
+        def grow(st, width=width):
+            outs["g"] = gb.gdn_tree_grow(offs_d, c_d, e_d, width, 16, dev_status=status, stream=st)
+
+        t_gr = timed(grow, reps=20)
+        gb.check_status(status)
+        t0 = time.perf_counter()
+        G.grow(offs, width, 16, c_np, e_np)
+        t_gcpu = time.perf_counter() - t0
+        print(json.dumps({"kind": "helper", "op": f"gdn_tree_grow (w = {width})", "workload": tb.name,
+                          "us": t_gr * 1e6, "node_tokens_per_s": tb.total_nodes / t_gr,
+                          "trees_per_s": tb.batch / t_gr,
+                          "bound": "latency (one block per request; a block-wide rank per step)",
+                          "cpu_baseline": {"kind": "oracle", "value": tb.total_nodes / t_gcpu,
+                                           "unit": "node-tokens/s", "cores": 1}}), flush=True)
     print(json.dumps({"kind": "helper", "op": "gdn_gather_rows x5 (q, k, v, g, beta)",
                       "workload": tb.name + "_shuffled", "us": t_g * 1e6, "bytes_moved": moved,
                       "achieved_gbs": moved / t_g / 1e9, "hbm_frac": moved / t_g / 1e9 / hbm_gbs}),

@@ -88,6 +88,8 @@ def lib():
         L.gdn_tree_commit.restype = ctypes.c_int
         L.gdn_tree_states.argtypes = [ctypes.POINTER(StatesArgs), _P]
         L.gdn_tree_states.restype = ctypes.c_int
+        L.gdn_tree_grow.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+        L.gdn_tree_grow.restype = ctypes.c_int
         L.gdn_tree_relabel.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]
         L.gdn_tree_relabel.restype = ctypes.c_int
         L.gdn_gather_rows.argtypes = [_P, _P, _P, _P, _I, _I, ctypes.c_int64, _P, _P]
@@ -192,6 +194,25 @@ def gdn_tree_states(k, v, g, beta, S0, node_offsets, parent, anc_mask, sel_reque
                    _ptr(sel_node), _ptr(out), _ptr(dev_status))
     _check(lib().gdn_tree_states(ctypes.byref(a), _stream(stream)))
     return out
+
+
+def gdn_tree_grow(node_offsets: torch.Tensor, n_children: torch.Tensor, draws: torch.Tensor,
+                  width: int, max_depth: int = 16, dev_status=None, stream=None):
+    """Top-w best-first trees: (parent [T] int32, score [T] float32, n_nodes [B] int32)."""
+    _dev(node_offsets, "node_offsets", torch.int32)
+    _dev(n_children, "n_children", torch.int32)
+    _dev(draws, "draws", torch.float32)
+    T = n_children.numel()
+    if draws.dim() != 2 or draws.shape[0] != T or not draws.is_contiguous():
+        raise ValueError("draws must be a contiguous [T, max_children] tensor")
+    B = node_offsets.numel() - 1
+    parent = torch.empty(T, dtype=torch.int32, device=draws.device)
+    score = torch.empty(T, dtype=torch.float32, device=draws.device)
+    n_nodes = torch.empty(B, dtype=torch.int32, device=draws.device)
+    _check(lib().gdn_tree_grow(_ptr(node_offsets), B, T, int(width), int(max_depth), draws.shape[1],
+                               _ptr(n_children), _ptr(draws), _ptr(parent), _ptr(score), _ptr(n_nodes),
+                               _ptr(dev_status), _stream(stream)))
+    return parent, score, n_nodes
 
 
 def gdn_tree_relabel(parent: torch.Tensor, node_offsets: torch.Tensor, max_nodes: int,

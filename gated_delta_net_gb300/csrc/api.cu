@@ -112,6 +112,24 @@ int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offsets, int3
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "build_desc launch");
 }
 
+int gdn_tree_grow(const int32_t *node_offsets, int32_t batch, int32_t total_nodes, int32_t width, int32_t max_depth,
+                  int32_t max_children, const int32_t *n_children, const float *draws, int32_t *parent, float *score,
+                  int32_t *n_nodes, int32_t *dev_status, void *stream) {
+    g_err[0] = 0;
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", total_nodes);
+    if (width < 1) return fail(GDN_ERR_INVALID_ARG, "width %d < 1", width);
+    if (max_depth < 1) return fail(GDN_ERR_INVALID_ARG, "max_depth %d < 1", max_depth);
+    if (max_children < 1 || max_children > 64)
+        return fail(GDN_ERR_INVALID_ARG, "max_children %d outside [1, 64]", max_children);
+    if (batch == 0) return GDN_OK;
+    if (!node_offsets || !n_children || !draws || !parent || !score || !n_nodes)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    cudaError_t e = gdn::launch_grow(node_offsets, batch, total_nodes, width, max_depth, max_children, n_children,
+                                     draws, parent, score, n_nodes, dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "grow launch");
+}
+
 int gdn_tree_relabel(const int32_t *parent_in, const int32_t *node_offsets, int32_t batch, int32_t total_nodes,
                      int32_t max_nodes, int32_t *order, int32_t *rank, int32_t *parent_out, int32_t *dev_status,
                      void *stream) {

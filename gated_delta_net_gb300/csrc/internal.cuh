@@ -43,6 +43,9 @@ cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream);
 cudaError_t launch_relabel(const int32_t *parent_in, const int32_t *node_offsets, int batch, int total,
                            int max_nodes, int32_t *order, int32_t *rank, int32_t *parent_out,
                            int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_grow(const int32_t *node_offsets, int batch, int total, int width, int max_depth, int max_children,
+                        const int32_t *n_children, const float *draws, int32_t *parent, float *score, int32_t *n_nodes,
+                        int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *src, void *dst, const int32_t *index, const int32_t *node_offsets,
                                int batch, int total, int64_t row_bytes, int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_verify_branches(const gdn_verify_args &a, cudaStream_t stream);

@@ -99,6 +99,32 @@ GDN_API int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offse
                         int32_t *depth, int32_t *dev_status, void *stream);
 
 /*
+ * gdn_tree_grow -- draft-tree construction ("Methodology", section 2 "Tree
+ * Construction": DySpec's best-first search, modified to expand the top-w
+ * nodes of the candidate heap together).  Per request, node 0 is the root
+ * (score 0, depth 1) and ids follow creation order.  One step takes the w best
+ * frontier nodes -- not yet expanded, depth < max_depth -- by score descending,
+ * then id ascending, and expands them in that order: node p gets children
+ * j = 0 .. c_p - 1 scored score_p - e_pj * (j + 1) (float32 multiply, then
+ * subtract), until the request's capacity is reached or the frontier is empty.
+ * The random draws are inputs:
+ *   node_offsets [B+1]: the capacity N_b of each request (<= 256 nodes);
+ *   n_children [T] int32: c_p for node p of its request (row lo + p), used if p
+ *              is expanded, clipped to [0, max_children];
+ *   draws [T][max_children] float32: e_pj >= 0, finite (a NaN gives an
+ *              unspecified tree);
+ *   parent [T] int32 (request-local; -1 for the root and for rows past the
+ *              built tree), score [T] float32 (-inf past the tree), n_nodes [B].
+ * The tree is topologically ordered and ready for gdn_tree_build_desc.
+ * 1 <= width, 1 <= max_depth, 1 <= max_children <= 64.  Integer results and
+ * scores are bit-exact against the float32 definition.
+ */
+GDN_API int gdn_tree_grow(const int32_t *node_offsets, int32_t batch, int32_t total_nodes, int32_t width,
+                          int32_t max_depth, int32_t max_children, const int32_t *n_children,
+                          const float *draws, int32_t *parent, float *score, int32_t *n_nodes,
+                          int32_t *dev_status, void *stream);
+
+/*
  * gdn_tree_relabel -- topological order for a tree given in any order (same
  * section, Solution bullet 1: the tree is processed parent before child).
  * Per request, nodes are sorted by (depth, old id), which is unique:

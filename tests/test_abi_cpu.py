@@ -25,7 +25,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gdn_gather_rows", "gdn_last_error", "gdn_tree_build_desc",
-                                         "gdn_tree_commit", "gdn_tree_relabel", "gdn_tree_states",
+                                         "gdn_tree_commit", "gdn_tree_grow", "gdn_tree_relabel",
+                                         "gdn_tree_states",
                                          "gdn_tree_verify", "gdn_tree_verify_branches",
                                          "gdn_tree_version"])
 
@@ -124,6 +125,17 @@ def test_states_rejects_bad_arguments(L, kw, code):
     a = _states_args(**kw)
     assert L.gdn_tree_states(ctypes.byref(a), None) == code
     assert L.gdn_tree_states(None, None) == binding.GDN_ERR_INVALID_ARG
+
+
+def test_grow_rejects_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    f = L.gdn_tree_grow
+    ok = [fake, 1, 8, 2, 16, 8, fake, fake, fake, fake, fake, None, None]
+    for pos, bad in ((1, -1), (2, -1), (3, 0), (4, 0), (5, 0), (5, 65), (6, None), (9, None)):
+        args = list(ok)
+        args[pos] = bad
+        assert f(*args) == binding.GDN_ERR_INVALID_ARG, pos
+    assert f(None, 0, 0, 1, 16, 8, None, None, None, None, None, None, None) == binding.GDN_OK
 
 
 def test_relabel_rejects_bad_arguments(L):
