@@ -40,12 +40,15 @@ constexpr int kMaxPath = 16;
 // shared memory (bytes from a 1024-aligned base)
 constexpr int OFF_TILE = 0;        // fp32 state tile (TMA, 4 x [128][32], 128B swizzle); also
                                    // S0 hi | lo as bf16 K-major tiles ([2][128][128 B] each)
-constexpr int OFF_KEYS = 65536;    // bf16 path keys [16][128], 128B swizzle (2 column blocks)
-constexpr int OFF_A = OFF_KEYS + 4096;  // A hi | lo: bf16 [128][16] core-matrix layout, 4 KB each
-constexpr int OFF_VP = OFF_A + 8192;    // fp32 path values [16][128]
-constexpr int OFF_COEF = OFF_VP + kMaxPath * kD * 4;  // fp32 [16][16]
-constexpr int OFF_SCAL = OFF_COEF + kMaxPath * kMaxPath * 4;  // bet, egam, fdec, gam [16]; pn [16]
-constexpr int OFF_MISC = OFF_SCAL + 5 * kMaxPath * 4;       // tmem slot, bad path flags [2]
+// path data is double-buffered: one item's is prepared while the previous item's
+// state tile is stored
+constexpr int OFF_KEYS = 65536;    // [2] bf16 path keys [16][128], 128B swizzle (2 column blocks), 4 KB each
+constexpr int OFF_A = OFF_KEYS + 8192;  // A hi | lo: bf16 [128][16] core-matrix layout, 4 KB each
+constexpr int OFF_VP = OFF_A + 8192;    // [2] fp32 path values [16][128]
+constexpr int OFF_COEF = OFF_VP + 2 * kMaxPath * kD * 4;  // fp32 [16][16]
+constexpr int OFF_SCAL = OFF_COEF + kMaxPath * kMaxPath * 4;  // [2] bet, egam, fdec, gam [16]; pn [16]
+constexpr int kScal = 5 * kMaxPath;                           // floats per buffer
+constexpr int OFF_MISC = OFF_SCAL + 2 * kScal * 4;            // tmem slot, bad path flags [2]
 constexpr int OFF_BAR = OFF_MISC + 16;
 constexpr int kSmemBytes = OFF_BAR + 3 * 8;
 
@@ -105,13 +108,9 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
                  TcCommitParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     float *tile = reinterpret_cast<float *>(sm + OFF_TILE);
-    float *vp = reinterpret_cast<float *>(sm + OFF_VP);
     float *coef = reinterpret_cast<float *>(sm + OFF_COEF);
-    float *bet = reinterpret_cast<float *>(sm + OFF_SCAL), *egam = bet + kMaxPath, *fdec = bet + 2 * kMaxPath,
-          *gam = bet + 3 * kMaxPath;
-    int *pn = reinterpret_cast<int *>(bet + 4 * kMaxPath);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
-    int *s_bad = reinterpret_cast<int *>(sm + OFF_MISC + 4);
+    int *s_bad = reinterpret_cast<int *>(sm + OFF_MISC + 4);     // [2], by path-data buffer
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);  // tile, W, U
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
@@ -138,50 +137,113 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     const uint32_t tmem = *tslot;
     bool ok = true;
     uint32_t ph_tile = 0, ph_mma = 0;  // completed phases of the tile and MMA barriers
-    int it = 0;                        // items committed by this block
+    int it = 0;                        // items committed by this block (path-data buffer = it & 1)
 
-    for (int idx = blockIdx.x; idx < p.items; idx += gridDim.x) {
-        const int hv = idx % p.hv_n, grp = idx / p.hv_n;
-        const int hk = hv / (p.hv_n / p.hk_n);
-        const int b = kSel ? __ldg(p.sel_req + grp) : grp;
-        if (kSel && (b < 0 || b >= p.batch)) {
-            if (tid == 0) flag(p.status, GDN_DEV_BAD_PATH);
-            continue;
+    struct Itm {
+        int b, hv, hk, lo, n, pa, L, sel;
+    };
+    // An item's parameters; false, with the status bit to raise, for one that is skipped.
+    auto params = [&](int idx, Itm &q, uint32_t (&mrow)[kMaxWords], int &err) -> bool {
+        q.hv = idx % p.hv_n;
+        const int grp = idx / p.hv_n;
+        q.hk = q.hv / (p.hv_n / p.hk_n);
+        q.b = kSel ? __ldg(p.sel_req + grp) : grp;
+        err = 0;
+        if (kSel && (q.b < 0 || q.b >= p.batch)) {
+            err = GDN_DEV_BAD_PATH;
+            return false;
         }
-        const int lo = p.offsets[b];
-        const int n = p.offsets[b + 1] - lo;
-        int L, pa = 0, sel = -1;
-        uint32_t mrow[kMaxWords];
+        q.lo = __ldg(p.offsets + q.b);
+        q.n = __ldg(p.offsets + q.b + 1) - q.lo;
+        q.pa = 0;
+        q.sel = -1;
         if constexpr (kSel) {
             // the selected node's path: the set bits of its ancestor-mask row
-            sel = __ldg(p.sel_node + grp);
-            if (sel < 0 || sel >= n || lo < 0 || lo + n > p.total) {
-                if (tid == 0) flag(p.status, GDN_DEV_BAD_PATH);
-                continue;
+            q.sel = __ldg(p.sel_node + grp);
+            if (q.sel < 0 || q.sel >= q.n || q.lo < 0 || q.lo + q.n > p.total) {
+                err = GDN_DEV_BAD_PATH;
+                return false;
             }
-            L = 0;
+            q.L = 0;
 #pragma unroll
             for (int w = 0; w < kMaxWords; ++w) {
-                mrow[w] = w < p.words ? __ldg(p.mask + (int64_t)(lo + sel) * p.words + w) : 0u;
-                L += __popc(mrow[w]);
+                mrow[w] = w < p.words ? __ldg(p.mask + (int64_t)(q.lo + q.sel) * p.words + w) : 0u;
+                q.L += __popc(mrow[w]);
             }
-            if (L > kMaxPath) {
-                if (tid == 0) flag(p.status, GDN_DEV_TOO_DEEP);
-                continue;
+            if (q.L > kMaxPath) {
+                err = GDN_DEV_TOO_DEEP;
+                return false;
             }
         } else {
-            pa = p.poff[b];
-            L = p.poff[b + 1] - pa;
-            if (L < 0 || L > kMaxPath || L > n || lo < 0 || lo + n > p.total) {
-                if (tid == 0) flag(p.status, L > kMaxPath && L <= n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
-                continue;
+            q.pa = __ldg(p.poff + q.b);
+            q.L = __ldg(p.poff + q.b + 1) - q.pa;
+            if (q.L < 0 || q.L > kMaxPath || q.L > q.n || q.lo < 0 || q.lo + q.n > p.total) {
+                err = q.L > kMaxPath && q.L <= q.n ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH;
+                return false;
             }
         }
-        const int row_in = (b * p.hv_n + hv) * kD, tile_row = idx * kD;
-        int *bad_flag = s_bad + (it & 1);
+        return true;
+    };
+    // An item's path data into buffer `buf` (whose bad flag reads zero): the path
+    // checked root first along parent -> child edges (and, for a selected node,
+    // ending at it), node ids, keys (bf16, 16-byte pieces, rows past L zero),
+    // values (fp32), raw g and beta.
+    auto prep = [&](const Itm &q, const uint32_t (&mrow)[kMaxWords], int buf) {
+        float *bet = reinterpret_cast<float *>(sm + OFF_SCAL) + buf * kScal, *gam = bet + 3 * kMaxPath;
+        int *pn = reinterpret_cast<int *>(bet + 4 * kMaxPath);
+        float *vp = reinterpret_cast<float *>(sm + OFF_VP) + buf * (kMaxPath * kD);
+        uint8_t *keys = sm + OFF_KEYS + buf * 4096;
+        auto node_at = [&](int t) -> int {
+            if constexpr (kSel) return nth_bit(mrow, p.words, t);
+            else return __ldg(p.pidx + q.pa + t);
+        };
+        if (kSel && q.L == 0 && tid == 0) atomicOr(s_bad + buf, 1);
+        if (tid < q.L) {
+            const int node = node_at(tid);
+            const int expect = tid == 0 ? -1 : node_at(tid - 1);
+            pn[tid] = node;
+            const bool in = node >= 0 && node < q.n;
+            if (!in || __ldg(p.parent + q.lo + node) != expect || (kSel && tid == q.L - 1 && node != q.sel))
+                atomicOr(s_bad + buf, 1);
+            if (in) {
+                gam[tid] = __ldg(p.g + (int64_t)(q.lo + node) * p.hv_n + q.hv);
+                bet[tid] = __ldg(p.beta + (int64_t)(q.lo + node) * p.hv_n + q.hv);
+            }
+        }
+        const int t = tid >> 4, c = tid & 15;
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+        if (t < q.L) {
+            const int node = node_at(t);
+            if (node >= 0 && node < q.n) {
+                const int64_t gnode = q.lo + node;
+                kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (gnode * p.hk_n + q.hk) * kD) + c);
+                vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (gnode * p.hv_n + q.hv) * kD) + c);
+            }
+        }
+        *reinterpret_cast<uint4 *>(keys + sw128(t, c * 8, kMaxPath)) = kv;
+        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+        float *vrow = vp + t * kD + c * 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            vrow[2 * e] = __uint_as_float(w[e] << 16);
+            vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+    };
+
+    int prepped = -1;  // the item whose path data is already in its buffer
+    for (int idx = blockIdx.x; idx < p.items; idx += gridDim.x) {
+        Itm q;
+        uint32_t mrow[kMaxWords];
+        int err;
+        if (!params(idx, q, mrow, err)) {
+            if (tid == 0) flag(p.status, err);
+            continue;
+        }
+        const int L = q.L, buf = it & 1;
+        const int row_in = (q.b * p.hv_n + q.hv) * kD, tile_row = idx * kD;
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar[0], kD * kD * 4);
-            for (int q = 0; q < 4; ++q) tma_load_2d(tile + q * kD * 32, &tmS0, &bar[0], q * 32, row_in);
+            for (int qq = 0; qq < 4; ++qq) tma_load_2d(tile + qq * kD * 32, &tmS0, &bar[0], qq * 32, row_in);
             const int nx = idx + (int)gridDim.x;  // the next item's state tile, into L2
             if (nx < p.items) {
                 const int nb = kSel ? __ldg(p.sel_req + nx / p.hv_n) : nx / p.hv_n;
@@ -189,50 +251,14 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
                     prefetch_l2(p.S0 + ((int64_t)nb * p.hv_n + nx % p.hv_n) * (kD * kD), kD * kD * 4);
             }
         }
-        // path validation: root first, parent -> child edges (and, for a selected
-        // node, a path that ends at that node)
-        if (kSel && L == 0 && tid == 0) atomicOr(bad_flag, 1);
-        if (tid < L) {
-            int node, expect;
-            if constexpr (kSel) {
-                node = nth_bit(mrow, p.words, tid);
-                expect = tid == 0 ? -1 : nth_bit(mrow, p.words, tid - 1);
-            } else {
-                node = p.pidx[pa + tid];
-                expect = tid == 0 ? -1 : p.pidx[pa + tid - 1];
-            }
-            pn[tid] = node;
-            if (node < 0 || node >= n || p.parent[lo + node] != expect || (kSel && tid == L - 1 && node != sel))
-                atomicOr(bad_flag, 1);
-        }
+        if (prepped != idx) prep(q, mrow, buf);
         __syncthreads();
-        const bool bad = *bad_flag != 0;
-        if (tid == 0) s_bad[(it & 1) ^ 1] = 0;  // the next item's flag starts clear
-
-        // path keys (bf16, 16-byte pieces; rows past L are zero) and values (fp32)
-        {
-            const int t = tid >> 4, c = tid & 15;
-            uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-            if (!bad && t < L) {
-                const int64_t node = lo + pn[t];
-                kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (node * p.hk_n + hk) * kD) + c);
-                vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (node * p.hv_n + hv) * kD) + c);
-            }
-            *reinterpret_cast<uint4 *>(sm + OFF_KEYS + sw128(t, c * 8, kMaxPath)) = kv;
-            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
-            float *vrow = vp + t * kD + c * 8;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                vrow[2 * e] = __uint_as_float(w[e] << 16);
-                vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            }
-            if (!bad && tid < L) {
-                const int64_t node = lo + pn[tid];
-                gam[tid] = p.g[node * p.hv_n + hv];
-                bet[tid] = p.beta[node * p.hv_n + hv];
-            }
-        }
-        __syncthreads();
+        const bool bad = s_bad[buf] != 0;
+        if (tid == 0) s_bad[buf ^ 1] = 0;  // the next item's flag starts clear
+        float *bet = reinterpret_cast<float *>(sm + OFF_SCAL) + buf * kScal, *egam = bet + kMaxPath,
+              *fdec = bet + 2 * kMaxPath, *gam = bet + 3 * kMaxPath;
+        const float *vp = reinterpret_cast<const float *>(sm + OFF_VP) + buf * (kMaxPath * kD);
+        uint8_t *keys = sm + OFF_KEYS + buf * 4096;
         if (tid == 0 && !bad) {
             float acc = 0.f;
             for (int t = 0; t < L; ++t) {
@@ -253,7 +279,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int m = lane * 4 + e;
-                    d = fmaf(bf16_at(sm + OFF_KEYS, sw128(t, m, kMaxPath)), bf16_at(sm + OFF_KEYS, sw128(s_, m, kMaxPath)), d);
+                    d = fmaf(bf16_at(keys, sw128(t, m, kMaxPath)), bf16_at(keys, sw128(s_, m, kMaxPath)), d);
                 }
                 d = warp_sum(d);
                 if (lane == 0) coef[t * kMaxPath + s_] = bet[t] * expf(gam[t] - gam[s_]) * d;
@@ -300,7 +326,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t ad = smem_desc(smem_u32(sm + OFF_TILE + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-                        const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS + (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, 2);
+                        const uint64_t bd = smem_desc(smem_u32(keys + (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, 2);
                         mma_bf16(tmem, ad, bd, id, part > 0 || ks > 0);
                     }
                 mma_commit(&bar[1]);
@@ -344,7 +370,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16_f32(128, 128) | (1u << 16);
-                const uint64_t bd = smem_desc(smem_u32(sm + OFF_KEYS), 2048, 1024, 2);
+                const uint64_t bd = smem_desc(smem_u32(keys), 2048, 1024, 2);
                 mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A), 128, 256, 0), bd, id, false);
                 mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A + 4096), 128, 256, 0), bd, id, true);
                 mma_commit(&bar[2]);
@@ -378,9 +404,21 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             if (bad) {
                 flag(p.status, kSel ? GDN_DEV_BAD_DESC : GDN_DEV_BAD_PATH);
             } else {
-                for (int q = 0; q < 4; ++q) tma_store_2d(&tmSN, tile + q * kD * 32, q * 32, tile_row);
+                for (int qq = 0; qq < 4; ++qq) tma_store_2d(&tmSN, tile + qq * kD * 32, qq * 32, tile_row);
                 bulk_commit();
                 bulk_wait_read();  // the tile space is free for the next item's load
+            }
+        }
+        // the next item's path data, into the other buffer, while the store above
+        // reads the tile out
+        const int nidx = idx + (int)gridDim.x;
+        if (nidx < p.items) {
+            Itm nq;
+            uint32_t nm[kMaxWords];
+            int nerr;
+            if (params(nidx, nq, nm, nerr)) {
+                prep(nq, nm, buf ^ 1);
+                prepped = nidx;
             }
         }
         ++it;
