@@ -146,14 +146,31 @@ verify_simt_kernel(SimtParams p) {
 
     // ---- phase 1: S0 read-out and right-hand side -------------------------
     float *kqw = smem + L.kq + warp * 2 * DK;
-    for (int i = warp; i < n; i += kWarps) {
+    // each warp's next node's k and q rows are requested while it works on the current one
+    float kn[EPL], qn[EPL];
+    auto kq_load = [&](int i) {
         const int64_t krow = ((int64_t)(lo + i) * p.hk_n + hk) * DK;
-        for (int m = lane; m < DK; m += 32) {
-            kqw[m] = load_f(kp, krow + m);
-            kqw[DK + m] = load_f(qp, krow + m);
+#pragma unroll
+        for (int r = 0; r < EPL; ++r) {
+            const int m = lane + 32 * r;
+            kn[r] = (i < n && m < DK) ? load_f(kp, krow + m) : 0.f;
+            qn[r] = (i < n && m < DK) ? load_f(qp, krow + m) : 0.f;
         }
+    };
+    kq_load(warp);
+    for (int i = warp; i < n; i += kWarps) {
+#pragma unroll
+        for (int r = 0; r < EPL; ++r) {
+            const int m = lane + 32 * r;
+            if (m < DK) {
+                kqw[m] = kn[r];
+                kqw[DK + m] = qn[r];
+            }
+        }
+        kq_load(i + kWarps);
         __syncwarp();
         if (lane < SW) {
+            const float vi = load_f(vp, ((int64_t)(lo + i) * p.hv_n + h) * p.dv + slab * SW + lane);
             float w = 0.f, z = 0.f;
             const float *srow = S0s + lane * (DK + 1);
 #pragma unroll 8
@@ -161,7 +178,6 @@ verify_simt_kernel(SimtParams p) {
                 w = fmaf(srow[m], kqw[m], w);
                 z = fmaf(srow[m], kqw[DK + m], z);
             }
-            const float vi = load_f(vp, ((int64_t)(lo + i) * p.hv_n + h) * p.dv + slab * SW + lane);
             Ub[i * SW + lane] = bet[i] * (vi - expf(gam[i]) * w);
             Zb[i * SW + lane] = z;
         }
@@ -184,22 +200,44 @@ verify_simt_kernel(SimtParams p) {
             const float gi = gam[i], bi = bet[i];
             float acc_u = lane < SW ? Ub[i * SW + lane] : 0.f;
             float acc_o = 0.f;
-            for (int j = par[i]; j >= 0; j = par[j]) {
-                const int64_t jrow = ((int64_t)(lo + j) * p.hk_n + hk) * DK;
-                float pk = 0.f, pq = 0.f;
+            // ancestors from the parent up, four at a time: their key rows are
+            // requested together, so a path costs one memory latency per four
+            // ancestors (the accumulation order is unchanged)
+            constexpr int kBatch = 4;
+            for (int j = par[i]; j >= 0;) {
+                int js[kBatch];
 #pragma unroll
-                for (int r = 0; r < EPL; ++r) {
-                    const int m = lane + 32 * r;
-                    const float kj = m < DK ? load_f(kp, jrow + m) : 0.f;
-                    pk = fmaf(kr[r], kj, pk);
-                    pq = fmaf(qr[r], kj, pq);
+                for (int u = 0; u < kBatch; ++u) {
+                    js[u] = j;
+                    if (j >= 0) j = par[j];
                 }
-                pk = warp_sum(pk);
-                pq = warp_sum(pq);
-                const float dec = expf(gi - gam[j]);
-                const float uj = lane < SW ? Ub[j * SW + lane] : 0.f;
-                acc_u -= bi * dec * pk * uj;
-                acc_o += dec * pq * uj;
+                float kj[kBatch][EPL];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int64_t jrow = ((int64_t)(lo + max(js[u], 0)) * p.hk_n + hk) * DK;
+#pragma unroll
+                    for (int r = 0; r < EPL; ++r) {
+                        const int m = lane + 32 * r;
+                        kj[u][r] = (js[u] >= 0 && m < DK) ? load_f(kp, jrow + m) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int ja = js[u];
+                    if (ja < 0) break;  // warp-uniform
+                    float pk = 0.f, pq = 0.f;
+#pragma unroll
+                    for (int r = 0; r < EPL; ++r) {
+                        pk = fmaf(kr[r], kj[u][r], pk);
+                        pq = fmaf(qr[r], kj[u][r], pq);
+                    }
+                    pk = warp_sum(pk);
+                    pq = warp_sum(pq);
+                    const float dec = expf(gi - gam[ja]);
+                    const float uj = lane < SW ? Ub[ja * SW + lane] : 0.f;
+                    acc_u -= bi * dec * pk * uj;
+                    acc_o += dec * pq * uj;
+                }
             }
             float self = 0.f;
 #pragma unroll
