@@ -367,6 +367,22 @@ def test_tc_path_forest_and_chain16():
     assert rel_err(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("shape", ["star", "binary", "all_roots"])
+def test_tc_path_tree_shapes(shape):
+    # extreme shapes of 128 nodes: one root with 127 children (every descendant
+    # row of the root full), a complete binary tree of depth 7, and 128 roots
+    if shape == "star":
+        par = np.array([-1] + [0] * 127, np.int32)
+    elif shape == "binary":
+        par = np.array([-1] + [(i - 1) // 2 for i in range(1, 127)], np.int32)
+    else:
+        par = np.full(128, -1, np.int32)
+    tb = _tc_batch(61, (len(par), len(par)), fn=lambda r, n: par)
+    o, status, _ = run_verify(tb)
+    gb.check_status(status)
+    assert rel_err(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
 def test_tc_path_fp32_output_and_scale():
     tb = _tc_batch(5, (128, 60))
     tb.scale = 0.25
