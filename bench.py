@@ -92,10 +92,15 @@ def verify_flops(tb) -> int:
 
 
 def source_sha(files) -> str:
+    """Hash of the kernel sources without // comments and blank lines, so that a
+    capture stays valid across comment-only edits and no longer after a code edit."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

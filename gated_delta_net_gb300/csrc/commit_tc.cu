@@ -12,8 +12,10 @@
 // chosen node (the path is the node's ancestor-mask row, root first), so that
 // a later commit of one of them needs no recompute.
 //
-// Persistent blocks (two per SM) walk the (request, value head) items; the next
-// item's state tile is requested into L2 while the current one is committed.
+// Persistent blocks (two per SM) walk the (request, value head) items.  The
+// next item's path data (keys, values, g, beta, node ids and their checks) is
+// prepared into a second buffer while thread 0 waits for the current state
+// tile's store, and the next tile is requested into L2.
 // Both contractions are GEMMs with a 16-wide side and run on tcgen05 with fp32
 // accumulation:
 //     W  = S0 K^T      M = 128 state rows, N = 16 path keys, K = 128

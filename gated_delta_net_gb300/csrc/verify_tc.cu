@@ -1,8 +1,8 @@
 // verify_tc.cu -- tcgen05/TMA tree verification for bf16 tokens, d_k = d_v = 128,
 // trees of at most 128 nodes and depth at most 16 (sm_103a).
 //
-// Computes, for one (request, value head) per thread block, the masked
-// triangular solve of "Trees from Marginals" (gist.science Technical Summary,
+// Computes, for each (request, value head) work item, the masked triangular
+// solve of "Trees from Marginals" (gist.science Technical Summary,
 // section 3 "Rollback-Free Tree Verification for GDN"):
 //     X = strict-ancestor mask * beta_i * D_ij * (K K^T),  Y = ancestor mask * D_ij * (Q K^T)
 //     (I + X) U = R = beta * (V - e^gamma * K S0^T)
@@ -27,8 +27,10 @@
 //   warps 4-7 ("state"): S0 conversion; right-hand side R rows; epilogue.
 //   thread 128 issues the TMA copies and the S0 and output MMAs, thread 0 the Gram.
 // The grid is persistent (two blocks per SM); a block walks its (request, value
-// head) items and overlaps the next item's tree metadata, K/Q tiles and S0
-// conversion with the current item's right-hand side, output MMA and epilogue.
+// head) items.  The next item's tree metadata is built during the current
+// item's right-hand side and epilogue, its K/Q tiles load once the output MMA
+// has consumed P and R, and its S0 conversion follows the epilogue (whose
+// staged rows occupy the S0 space), overlapping its own Gram and scatter.
 // Every mbarrier completes once per item, so waits use the item's parity.
 // A node whose right-hand side row turns non-finite has that row replaced by
 // zero in the output product and its subtree's outputs set to NaN, so

@@ -94,3 +94,14 @@ def test_clock_summary_keeps_only_the_timed_window():
     s = bench.summarize_clocks(lines, t0 + 100, t0 + 101)
     assert s["window"] == "around the timed region" and s["samples"] == 5
     assert bench.summarize_clocks([]) is None
+
+
+def test_source_hash_ignores_comments(tmp_path, monkeypatch):
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "a.cu").write_text("int x = 1;  // one\n\n// note\nint y;\n")
+    h1 = bench.source_sha(["a.cu"])
+    (tmp_path / "a.cu").write_text("int x = 1;  // changed words\n// another note\nint y;\n")
+    assert bench.source_sha(["a.cu"]) == h1
+    (tmp_path / "a.cu").write_text("int x = 2;\nint y;\n")
+    assert bench.source_sha(["a.cu"]) != h1
