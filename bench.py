@@ -70,6 +70,16 @@ def commit_bytes(tb) -> int:
             + 8 * (tb.batch + 1))
 
 
+def fused_bytes(tb) -> int:
+    """gdn_tree_commit_verify: the verify bytes (one S0 read) plus the committed
+    state's write and the accepted path's tokens."""
+    esz = 2 if tb.qkv_dtype == "bf16" else 4
+    L = len(tb.path_idx)
+    return (verify_bytes(tb) + tb.batch * tb.n_v_heads * tb.d_v * tb.d_k * 4
+            + L * (tb.n_k_heads * tb.d_k * esz + tb.n_v_heads * tb.d_v * esz + tb.n_v_heads * 8 + 8)
+            + 8 * (tb.batch + 1))
+
+
 def desc_bytes(tb) -> int:
     words = max(1, (tb.max_nodes + 31) // 32)
     return tb.total_nodes * (4 + 4 + 4 * words) + 4 * (tb.batch + 1)
@@ -261,15 +271,24 @@ def run_ours(args, rank, world, local_rank):
                                status, stream)
         if ev is not None:
             ev[0].record(stream)
-        gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
-                           d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                           out=o, dev_status=status, stream=stream)
+        if args.fused:
+            # the commit of the previous tree's accepted path (here the same tree's)
+            # fused with this tree's verification
+            gb.gdn_tree_commit_verify(d, d["S0"], tb.max_nodes, tb.max_depth_bound, d["q"], d["k"],
+                                      d["v"], d["g"], d["beta"], d["node_offsets"], d["parent"], mask,
+                                      depth, tb.max_nodes, max_depth=tb.max_depth_bound, S_new=S_new,
+                                      out=o, dev_status=status, stream=stream)
+        else:
+            gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                               d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                               out=o, dev_status=status, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
-                           d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes,
-                           max_path=tb.max_depth_bound, out=S_new, dev_status=status,
-                           stream=stream)
+        if not args.fused:
+            gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                               d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes,
+                               max_path=tb.max_depth_bound, out=S_new, dev_status=status,
+                               stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -343,12 +362,20 @@ def run_ours(args, rank, world, local_rank):
         bj = bufs[j]
         gb.gdn_tree_build_desc(bj["parent"], bj["node_offsets"], tb.max_nodes, mask, depth, words,
                                status, stream)
-        gb.gdn_tree_verify(bj["q"], bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
-                           bj["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                           out=obufs[j], dev_status=status, stream=stream)
-        gb.gdn_tree_commit(bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
-                           bj["parent"], bj["path_offsets"], bj["path_idx"], tb.max_nodes,
-                           max_path=tb.max_depth_bound, out=state, dev_status=status, stream=stream)
+        if args.fused:
+            # commit the previous step's accepted path, then verify this step's tree
+            bp = bufs[(it - 1) % 2] if it > 0 else bj
+            gb.gdn_tree_commit_verify(bp, state, tb.max_nodes, tb.max_depth_bound, bj["q"], bj["k"],
+                                      bj["v"], bj["g"], bj["beta"], bj["node_offsets"], bj["parent"],
+                                      mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                                      S_new=state, out=obufs[j], dev_status=status, stream=stream)
+        else:
+            gb.gdn_tree_verify(bj["q"], bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
+                               bj["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                               out=obufs[j], dev_status=status, stream=stream)
+            gb.gdn_tree_commit(bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
+                               bj["parent"], bj["path_offsets"], bj["path_idx"], tb.max_nodes,
+                               max_path=tb.max_depth_bound, out=state, dev_status=status, stream=stream)
         ev_done[it].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[it])
@@ -363,10 +390,10 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     hbm_gbs, bf16_tf, peak_kind = load_peaks()
-    vbytes = verify_bytes(tb)
+    vbytes = fused_bytes(tb) if args.fused else verify_bytes(tb)
     v_s = statistics.mean(verify_ms) / 1e3
     achieved = vbytes / v_s / 1e9
-    kernel = dominant_kernel(tb)
+    kernel = "verify_tc_fused" if args.fused else dominant_kernel(tb)
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
@@ -384,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
                    "tree": "random parent over nodes of depth < 16 (depth <= 16)",
                    "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
                    "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
-                   "step": "build_desc + verify + commit",
+                   "step": ("build_desc + commit_verify (the previous accepted path committed, "
+                            "fused with the verification)") if args.fused else "build_desc + verify + commit",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
@@ -394,7 +422,8 @@ def run_ours(args, rank, world, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "verify_only": {"us_per_launch": v_s * 1e6, "node_tokens_per_s": T / v_s,
                         "tflops": verify_flops(tb) / v_s / 1e12},
-        "step_bytes": {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)},
+        "step_bytes": ({"desc": desc_bytes(tb), "commit_verify": vbytes} if args.fused else
+                       {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)}),
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -402,7 +431,7 @@ def run_ours(args, rank, world, local_rank):
                 "pipeline": "serving loop: state resident and committed in place; per step "
                             "q/k/v/g/beta + tree uploaded from pinned memory and o read back; "
                             "upload, compute and read-back on three streams, two buffer sets"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if args.fused else 3) * args.steps,
         "clocks": clk.summary(),
     }
 
@@ -647,6 +676,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
+    ap.add_argument("--fused", action="store_true",
+                    help="step = build_desc + gdn_tree_commit_verify (commit fused into the verify)")
     ap.add_argument("--sweep", action="store_true",
                     help="time fused verify against the per-branch baseline over the sweep grid")
     ap.add_argument("--sweep-reps", type=int, default=10)

@@ -86,6 +86,8 @@ def lib():
             fn.restype = ctypes.c_int
         L.gdn_tree_commit.argtypes = [ctypes.POINTER(CommitArgs), _P]
         L.gdn_tree_commit.restype = ctypes.c_int
+        L.gdn_tree_commit_verify.argtypes = [ctypes.POINTER(CommitArgs), ctypes.POINTER(VerifyArgs), _P]
+        L.gdn_tree_commit_verify.restype = ctypes.c_int
         L.gdn_tree_states.argtypes = [ctypes.POINTER(StatesArgs), _P]
         L.gdn_tree_states.restype = ctypes.c_int
         L.gdn_tree_grow.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
@@ -306,10 +308,8 @@ def gdn_tree_verify_branches(q, k, v, g, beta, S0, node_offsets, parent, anc_mas
     return out
 
 
-def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_idx,
-                    max_nodes: int, max_path: int = 0, out=None, dev_status=None,
-                    stream=None) -> torch.Tensor:
-    """State after each request's accepted path [B, Hv, d_v, d_k]; ``out`` may be ``S0``."""
+def _commit_args(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_idx, max_nodes,
+                 max_path, out, dev_status):
     for name, t in (("k", k), ("v", v)):
         _dev(t, name)
     for name, t in (("g", g), ("beta", beta), ("S0", S0)):
@@ -332,8 +332,33 @@ def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_
                    _ptr(node_offsets), _ptr(k),
                    _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(parent), _ptr(path_offsets),
                    _ptr(pidx), _ptr(out), _ptr(dev_status))
+    return a, out, pidx
+
+
+def gdn_tree_commit(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_idx,
+                    max_nodes: int, max_path: int = 0, out=None, dev_status=None,
+                    stream=None) -> torch.Tensor:
+    """State after each request's accepted path [B, Hv, d_v, d_k]; ``out`` may be ``S0``."""
+    a, out, _keep = _commit_args(k, v, g, beta, S0, node_offsets, parent, path_offsets, path_idx,
+                                 max_nodes, max_path, out, dev_status)
     _check(lib().gdn_tree_commit(ctypes.byref(a), _stream(stream)))
     return out
+
+
+def gdn_tree_commit_verify(prev: dict, S0, max_nodes_prev: int, max_path: int,
+                           q, k, v, g, beta, node_offsets, parent, anc_mask, depth, max_nodes: int,
+                           max_depth: int = 16, scale: float = 1.0, S_new=None, out=None,
+                           out_dtype=None, dev_status=None, stream=None):
+    """Commit S0 along the previous tree's accepted path (``prev``: k, v, g, beta,
+    node_offsets, parent, path_offsets, path_idx), write it to ``S_new`` (may be
+    ``S0``), and verify the new tree from it.  Returns (o, S_new)."""
+    c, S_new, _keep = _commit_args(prev["k"], prev["v"], prev["g"], prev["beta"], S0,
+                                   prev["node_offsets"], prev["parent"], prev["path_offsets"],
+                                   prev["path_idx"], max_nodes_prev, max_path, S_new, dev_status)
+    a, out = _verify_args(q, k, v, g, beta, S_new, node_offsets, parent, anc_mask, depth, max_nodes,
+                          max_depth, scale, out, out_dtype, dev_status)
+    _check(lib().gdn_tree_commit_verify(ctypes.byref(c), ctypes.byref(a), _stream(stream)))
+    return out, S_new
 
 
 # ----------------------------------------------------------------------------

@@ -203,6 +203,30 @@ int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
 }
 
+int gdn_tree_commit_verify(const gdn_commit_args *c, const gdn_verify_args *v, void *stream) {
+    g_err[0] = 0;
+    if (!c) return fail(GDN_ERR_INVALID_ARG, "commit args are NULL");
+    int st = check_verify(v);
+    if (st) return st;
+    st = check_common(c->batch, c->n_k_heads, c->n_v_heads, c->d_k, c->d_v, c->max_nodes);
+    if (st) return st;
+    if (!valid_dtype(c->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", c->qkv_dtype);
+    if (c->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", c->total_nodes);
+    if (c->max_path < 0) return fail(GDN_ERR_INVALID_ARG, "max_path %d < 0", c->max_path);
+    if (c->batch != v->batch || c->n_k_heads != v->n_k_heads || c->n_v_heads != v->n_v_heads)
+        return fail(GDN_ERR_INVALID_ARG, "commit and verify shapes differ");
+    if (v->batch == 0) return GDN_OK;
+    if (!c->node_offsets || !c->k || !c->v || !c->g || !c->beta || !c->S0 || !c->parent ||
+        !c->path_offsets || !c->path_idx || !c->S_new)
+        return fail(GDN_ERR_INVALID_ARG, "a required commit pointer is NULL");
+    if (!gdn::commit_verify_tc_supported(*c, *v))
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "commit_verify: bf16 tokens, d = 128, max_nodes <= 128, max_depth and max_path in [1, 16], "
+                    "16-byte aligned tensors only");
+    cudaError_t e = gdn::launch_commit_verify_tc(*c, *v, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit_verify launch");
+}
+
 int gdn_tree_states(const gdn_states_args *a, void *stream) {
     g_err[0] = 0;
     if (!a) return fail(GDN_ERR_INVALID_ARG, "args is NULL");

@@ -88,4 +88,9 @@ cudaError_t ensure_smem(Kernel kern, int bytes, int (&have)[16]) {
 bool verify_tc_supported(const gdn_verify_args &a);
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream);
 
+// the same kernel committing each item's state along the previous tree's
+// accepted path first and verifying the new tree from the committed state
+bool commit_verify_tc_supported(const gdn_commit_args &c, const gdn_verify_args &a);
+cudaError_t launch_commit_verify_tc(const gdn_commit_args &c, const gdn_verify_args &a, cudaStream_t stream);
+
 }  // namespace gdn

@@ -25,7 +25,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     assert declared_symbols() == sorted(["gdn_gather_rows", "gdn_last_error", "gdn_tree_build_desc",
-                                         "gdn_tree_commit", "gdn_tree_grow", "gdn_tree_relabel",
+                                         "gdn_tree_commit", "gdn_tree_commit_verify", "gdn_tree_grow",
+                                         "gdn_tree_relabel",
                                          "gdn_tree_states",
                                          "gdn_tree_verify", "gdn_tree_verify_branches",
                                          "gdn_tree_version"])

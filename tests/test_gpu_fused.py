@@ -1,0 +1,111 @@
+"""GPU parity of gdn_tree_commit_verify: the delayed commit of the previous
+tree's accepted path fused with the verification of the next tree ("Trees from
+Marginals", gist.science Technical Summary, section 3, Solution, bullet 4: the
+state is committed in the next decoding iteration).
+
+Reference: oracle.commit on the previous tree (the committed state, fp32
+tolerance 1e-4 * max|S|), then oracle.verify of the new tree from that state
+(bf16 tolerance 2e-2 * max|o|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_net_gb300 import binding as gb
+from gated_delta_net_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_STATE, TOL_BF16 = 1e-4, 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_delta_net_gb300 import build
+    build.build()
+    gb.lib()
+
+
+def _rel(got, ref):
+    return float(np.max(np.abs(got - ref))) / max(float(np.max(np.abs(ref))), 1e-30)
+
+
+def _run(prev, new, in_place=False, S_new_init=None):
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S0 = dp["S0"]
+    S_new = S0 if in_place else (S_new_init if S_new_init is not None else torch.empty_like(S0))
+    S0_before = S0.clone()
+    o, S = gb.gdn_tree_commit_verify(dp, S0, prev.max_nodes, 16, dn["q"], dn["k"], dn["v"], dn["g"],
+                                     dn["beta"], dn["node_offsets"], dn["parent"], mask, depth,
+                                     new.max_nodes, max_depth=16, S_new=S_new, dev_status=status)
+    torch.cuda.synchronize()
+    return o, S, status, S0_before
+
+
+def _reference(prev, new):
+    S_ref, st = oracle.commit(prev)
+    assert st == 0
+    new.S0 = S_ref                 # the new tree is verified from the committed state
+    return S_ref, oracle.verify(new)
+
+
+def test_commit_then_verify_matches_the_oracle():
+    prev, new = W.serving_target(seed=21, batch=6), W.serving_target(seed=22, batch=6)
+    o, S, status, _ = _run(prev, new)
+    gb.check_status(status)
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_in_place_and_ragged_many_items():
+    # 80 requests x 32 value heads: several items per persistent block; ragged
+    # trees on both sides; the state committed in place
+    prev = W.ragged_serving(seed=23, batch=80)
+    new = W.ragged_serving(seed=24, batch=80)
+    o, S, status, S0_before = _run(prev, new, in_place=True)
+    gb.check_status(status)
+    prev.S0 = S0_before.cpu().numpy()
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_empty_previous_path_keeps_the_state_exactly():
+    parents = [W.depth_capped_random_tree(np.random.default_rng(s), 40, 16) for s in range(3)]
+    prev = W.custom(25, parents, n_k_heads=2, n_v_heads=4, d=128, qkv_dtype="bf16", path_fn=lambda p, r: [])
+    new = W.custom(26, parents, n_k_heads=2, n_v_heads=4, d=128, qkv_dtype="bf16")
+    o, S, status, S0_before = _run(prev, new)
+    gb.check_status(status)
+    assert torch.equal(S, S0_before)
+    new.S0 = S0_before.cpu().numpy().astype(np.float64)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
+
+
+def test_bad_previous_path_is_flagged_and_left_unwritten():
+    parent = W.depth_capped_random_tree(np.random.default_rng(3), 30, 16)
+    parents = [parent, parent, parent]
+    assert parent[0] == -1 and parent[1] == 0
+    paths = iter([[0, 1], [1], [0]])            # the second is not root-first
+    prev = W.custom(27, parents, n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16",
+                    path_fn=lambda p, r: next(paths))
+    new = W.custom(28, parents, n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16")
+    sentinel = torch.full((3, 2, 128, 128), 3.0, device="cuda")
+    dn = gb.upload(new)
+    o_init = torch.full((new.total_nodes, 2, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    dp = gb.upload(prev)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], 30, dev_status=status)
+    gb.gdn_tree_commit_verify(dp, dp["S0"], 30, 16, dn["q"], dn["k"], dn["v"], dn["g"], dn["beta"],
+                              dn["node_offsets"], dn["parent"], mask, depth, 30, S_new=sentinel,
+                              out=o_init, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+    assert torch.all(sentinel[1] == 3.0)
+    assert torch.all(o_init[30:60] == 5.0)
+    assert not torch.all(sentinel[0] == 3.0) and not torch.all(o_init[:30] == 5.0)
