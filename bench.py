@@ -40,6 +40,7 @@ L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
+    "verify_tc_fused": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
     "verify_simt": ["gated_delta_net_gb300/csrc/verify_simt.cu"],
     "commit_tc": ["gated_delta_net_gb300/csrc/commit_tc.cu"],
 }
@@ -334,7 +335,10 @@ def run_ours(args, rank, world, local_rank):
     in_keys = ["q", "k", "v", "g", "beta", "node_offsets", "parent", "path_offsets", "path_idx"]
     h2d = sum(h[k].numel() * h[k].element_size() for k in in_keys)
     d2h = o.numel() * o.element_size()
-    bufs = [{k: torch.empty_like(d[k]) for k in in_keys} for _ in range(2)]
+    # the fused step still reads the previous step's tree (its accepted path),
+    # so it cycles three input sets instead of two
+    nset = 3 if args.fused else 2
+    bufs = [{k: torch.empty_like(d[k]) for k in in_keys} for _ in range(nset)]
     obufs = [torch.empty_like(o) for _ in range(2)]
     o_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
     state = d["S0"].clone()
@@ -349,10 +353,10 @@ def run_ours(args, rank, world, local_rank):
     for it in range(e2e_steps + warm):
         if it == warm:
             t_start.record(up)
-        j = it % 2
+        j, jo = it % nset, it % 2
         with torch.cuda.stream(up):
             if it >= 2:
-                up.wait_event(ev_done[it - 2])          # buffer set j is free again
+                up.wait_event(ev_done[it - 2])          # input set j is free again
             for k in in_keys:
                 bufs[j][k].copy_(h[k], non_blocking=True)
             ev_in[it].record(up)
@@ -364,22 +368,22 @@ def run_ours(args, rank, world, local_rank):
                                status, stream)
         if args.fused:
             # commit the previous step's accepted path, then verify this step's tree
-            bp = bufs[(it - 1) % 2] if it > 0 else bj
+            bp = bufs[(it - 1) % nset] if it > 0 else bj
             gb.gdn_tree_commit_verify(bp, state, tb.max_nodes, tb.max_depth_bound, bj["q"], bj["k"],
                                       bj["v"], bj["g"], bj["beta"], bj["node_offsets"], bj["parent"],
                                       mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                                      S_new=state, out=obufs[j], dev_status=status, stream=stream)
+                                      S_new=state, out=obufs[jo], dev_status=status, stream=stream)
         else:
             gb.gdn_tree_verify(bj["q"], bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
                                bj["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                               out=obufs[j], dev_status=status, stream=stream)
+                               out=obufs[jo], dev_status=status, stream=stream)
             gb.gdn_tree_commit(bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
                                bj["parent"], bj["path_offsets"], bj["path_idx"], tb.max_nodes,
                                max_path=tb.max_depth_bound, out=state, dev_status=status, stream=stream)
         ev_done[it].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[it])
-            o_h[j].copy_(obufs[j], non_blocking=True)
+            o_h[jo].copy_(obufs[jo], non_blocking=True)
             ev_out[it].record(down)
     t_end.record(down)
     torch.cuda.synchronize()

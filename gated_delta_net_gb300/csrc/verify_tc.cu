@@ -421,43 +421,61 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             if (lane == 0) coef[t * kMaxDepth + s_] = cbet[t] * expf(cgam[t] - cgam[s_]) * d;
         }
         named_sync(2, 128);
-        // this thread's row: W_t over 16-column chunks (keys read as broadcasts)
+        // this thread's row: W_t over 16-column chunks (keys read as broadcasts);
+        // the t loops stop at the path length (uniform over the block) and the
+        // next chunk of the row is loaded while this one is used
         const float *srow = p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD) + (int64_t)st * kD;
+        auto load_chunk = [&](int c0, float4 (&f)[4]) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) f[q] = __ldg(reinterpret_cast<const float4 *>(srow + c0) + q);
+        };
+        auto unpack = [](const float4 (&f)[4], float (&x)[16]) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                x[q * 4 + 0] = f[q].x; x[q * 4 + 1] = f[q].y; x[q * 4 + 2] = f[q].z; x[q * 4 + 3] = f[q].w;
+            }
+        };
         float W[kMaxDepth];
 #pragma unroll
         for (int t = 0; t < kMaxDepth; ++t) W[t] = 0.f;
+        float4 nxt[4];
+        load_chunk(0, nxt);
 #pragma unroll 1
         for (int c0 = 0; c0 < kD; c0 += 16) {
             float x[16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f4 = __ldg(reinterpret_cast<const float4 *>(srow + c0) + q);
-                x[q * 4 + 0] = f4.x; x[q * 4 + 1] = f4.y; x[q * 4 + 2] = f4.z; x[q * 4 + 3] = f4.w;
-            }
+            unpack(nxt, x);
+            if (c0 + 16 < kD) load_chunk(c0 + 16, nxt);
 #pragma unroll
             for (int t = 0; t < kMaxDepth; ++t) {
-                const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
-                const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
-                const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                float w = W[t];
+                if (t < Lc) {
+                    const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
+                    const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
+                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                    float w = W[t];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    w = fmaf(x[2 * e], bf16_lo(kw[e]), w);
-                    w = fmaf(x[2 * e + 1], bf16_hi(kw[e]), w);
+                    for (int e = 0; e < 8; ++e) {
+                        w = fmaf(x[2 * e], bf16_lo(kw[e]), w);
+                        w = fmaf(x[2 * e + 1], bf16_hi(kw[e]), w);
+                    }
+                    W[t] = w;
                 }
-                W[t] = w;
             }
         }
+        // the second pass re-reads the row from the start
+        load_chunk(0, nxt);
         // the chain for this row, then A_t = e^(gamma_L - gamma_t) u_t
         float A[kMaxDepth];
         {
             const __nv_bfloat16 *vcol = p.c_v + (int64_t)it.hv * kD + st;
+            float vt[kMaxDepth];
+#pragma unroll
+            for (int t = 0; t < kMaxDepth; ++t)
+                vt[t] = t < Lc ? __bfloat162float(vcol[(int64_t)cnode[t] * p.hv_n * kD]) : 0.f;
 #pragma unroll
             for (int t = 0; t < kMaxDepth; ++t) {
                 float u = 0.f;
                 if (t < Lc) {
-                    const float vt = __bfloat162float(vcol[(int64_t)cnode[t] * p.hv_n * kD]);
-                    u = cbet[t] * (vt - cegam[t] * W[t]);
+                    u = cbet[t] * (vt[t] - cegam[t] * W[t]);
 #pragma unroll
                     for (int s2 = 0; s2 < t; ++s2) u = fmaf(-coef[t * kMaxDepth + s2], A[s2], u);
                 }
@@ -471,22 +489,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll 1
         for (int c0 = 0; c0 < kD; c0 += 16) {
             float x[16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f4 = __ldg(reinterpret_cast<const float4 *>(srow + c0) + q);
-                x[q * 4 + 0] = f4.x; x[q * 4 + 1] = f4.y; x[q * 4 + 2] = f4.z; x[q * 4 + 3] = f4.w;
-            }
+            unpack(nxt, x);
+            if (c0 + 16 < kD) load_chunk(c0 + 16, nxt);
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] *= eL;
 #pragma unroll
             for (int t = 0; t < kMaxDepth; ++t) {
-                const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
-                const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
-                const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                if (t < Lc) {
+                    const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
+                    const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
+                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[2 * e] = fmaf(A[t], bf16_lo(kw[e]), x[2 * e]);
-                    x[2 * e + 1] = fmaf(A[t], bf16_hi(kw[e]), x[2 * e + 1]);
+                    for (int e = 0; e < 8; ++e) {
+                        x[2 * e] = fmaf(A[t], bf16_lo(kw[e]), x[2 * e]);
+                        x[2 * e + 1] = fmaf(A[t], bf16_hi(kw[e]), x[2 * e + 1]);
+                    }
                 }
             }
             if (!err) {
