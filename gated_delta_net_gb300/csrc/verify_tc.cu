@@ -23,14 +23,16 @@
 //
 // Warp roles, handing off through mbarriers rather than block-wide barriers:
 //   warps 0-3 ("tree"):  node metadata, paths, gamma; scatter of the Gram into
-//                        per-node ancestor rows; X scaling; P; P rows.
+//                        per-node ancestor rows (X and Y); X scaling; P; P rows.
 //   warps 4-7 ("state"): S0 conversion; right-hand side R rows; epilogue.
+//                        (In the fused kernel they also commit the state and
+//                        scatter Y, whose rows hold the path keys meanwhile.)
 //   thread 128 issues the TMA copies and the S0 and output MMAs, thread 0 the Gram.
 // The grid is persistent (two blocks per SM); a block walks its (request, value
 // head) items.  The next item's tree metadata is built during the current
 // item's right-hand side and epilogue, its K/Q tiles load once the output MMA
 // has consumed P and R, and its S0 conversion follows the epilogue (whose
-// staged rows occupy the S0 space), overlapping its own Gram and scatter.
+// staged rows occupy the S0 space), overlapping its own Gram and scatters.
 // Every mbarrier completes once per item, so waits use the item's parity.
 // A node whose right-hand side row turns non-finite has that row replaced by
 // zero in the output product and its subtree's outputs set to NaN, so
@@ -601,10 +603,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
             for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0x7Fu) : i;
 
-            // strict part of the Gram -> raw X rows
+            // strict part of the Gram -> raw X rows, full part -> raw Y rows; the
+            // state warps meanwhile convert this item's S0
             ok = mbar_wait(&bar[B_GRAM], ph) && ok;
             tc_fence_after();
             scatter(0, Xs, true);
+            if constexpr (!kFused) scatter(128, Ys, false);
             tc_fence_before();
             mbar_arrive(&bar[B_TFREE]);
 
@@ -669,12 +673,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             cur = nx;
         } else {
             // ===================== state warps =================================
-            // full part of the Gram -> raw Y rows
+            // (fused kernel) full part of the Gram -> raw Y rows
             ok = mbar_wait(&bar[B_DESC], ph) && ok;
-            ok = mbar_wait(&bar[B_GRAM], ph) && ok;
-            tc_fence_after();
-            scatter(128, Ys, false);
-            tc_fence_before();
+            if constexpr (kFused) {
+                ok = mbar_wait(&bar[B_GRAM], ph) && ok;
+                tc_fence_after();
+                scatter(128, Ys, false);
+                tc_fence_before();
+            }
             mbar_arrive(&bar[B_TFREE]);
 
             if (issuer) {
