@@ -40,7 +40,6 @@ L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
-    "verify_tc_fused": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
     "verify_simt": ["gated_delta_net_gb300/csrc/verify_simt.cu"],
     "commit_tc": ["gated_delta_net_gb300/csrc/commit_tc.cu"],
 }
@@ -67,16 +66,6 @@ def commit_bytes(tb) -> int:
     esz = 2 if tb.qkv_dtype == "bf16" else 4
     L = len(tb.path_idx)
     return (2 * tb.batch * tb.n_v_heads * tb.d_v * tb.d_k * 4
-            + L * (tb.n_k_heads * tb.d_k * esz + tb.n_v_heads * tb.d_v * esz + tb.n_v_heads * 8 + 8)
-            + 8 * (tb.batch + 1))
-
-
-def fused_bytes(tb) -> int:
-    """gdn_tree_commit_verify: the verify bytes (one S0 read) plus the committed
-    state's write and the accepted path's tokens."""
-    esz = 2 if tb.qkv_dtype == "bf16" else 4
-    L = len(tb.path_idx)
-    return (verify_bytes(tb) + tb.batch * tb.n_v_heads * tb.d_v * tb.d_k * 4
             + L * (tb.n_k_heads * tb.d_k * esz + tb.n_v_heads * tb.d_v * esz + tb.n_v_heads * 8 + 8)
             + 8 * (tb.batch + 1))
 
@@ -272,24 +261,27 @@ def run_ours(args, rank, world, local_rank):
                                status, stream)
         if ev is not None:
             ev[0].record(stream)
-        if args.fused:
-            # the commit of the previous tree's accepted path (here the same tree's)
-            # fused with this tree's verification
-            gb.gdn_tree_commit_verify(d, d["S0"], tb.max_nodes, tb.max_depth_bound, d["q"], d["k"],
-                                      d["v"], d["g"], d["beta"], d["node_offsets"], d["parent"], mask,
-                                      depth, tb.max_nodes, max_depth=tb.max_depth_bound, S_new=S_new,
-                                      out=o, dev_status=status, stream=stream)
-        else:
-            gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
-                               d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                               out=o, dev_status=status, stream=stream)
+        gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                           d["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                           out=o, dev_status=status, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        if not args.fused:
-            gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
-                               d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes,
-                               max_path=tb.max_depth_bound, out=S_new, dev_status=status,
-                               stream=stream)
+        gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                           d["parent"], d["path_offsets"], d["path_idx"], tb.max_nodes,
+                           max_path=tb.max_depth_bound, out=S_new, dev_status=status,
+                           stream=stream)
+
+    def serving_step():
+        # the serving order of one decoding iteration: the previous tree's accepted
+        # path committed (here the same synthetic tree's), then the new tree verified
+        # from the committed state; one call, the verification launched as the
+        # commit's programmatic dependent
+        gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes, mask, depth, words,
+                               status, stream)
+        gb.gdn_tree_commit_verify(d, d["S0"], tb.max_nodes, tb.max_depth_bound, d["q"], d["k"],
+                                  d["v"], d["g"], d["beta"], d["node_offsets"], d["parent"], mask,
+                                  depth, tb.max_nodes, max_depth=tb.max_depth_bound, S_new=S_new,
+                                  out=o, dev_status=status, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -325,19 +317,40 @@ def run_ours(args, rank, world, local_rank):
     value = job_throughput(T, args.steps, total_s, world)
     ms_per_step = total_s * 1e3 / args.steps
 
+    # the same work in the serving order (desc, then commit and verify chained in
+    # one call), timed the same way
+    for _ in range(args.warmup):
+        flush.zero_()
+        serving_step()
+    torch.cuda.synchronize()
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for e in sevs:
+        flush.zero_()
+        e[0].record(stream)
+        serving_step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    serving_s = reduce_max(sum(e[0].elapsed_time(e[1]) for e in sevs) / 1e3, dev)
+
     # End to end through the public API, as a serving loop: the recurrent state
-    # stays resident and is committed in place; every step uploads its inputs
-    # (the tree's q, k, v, g, beta and its structure) from pinned host memory
-    # and reads its outputs o back.  Uploads, compute and read-backs run on three
-    # streams with two input/output buffer sets, so step k + 1's upload overlaps
+    # stays resident; every step uploads its inputs (the tree's q, k, v, g, beta,
+    # its structure and accepted path) from pinned host memory, commits the
+    # previous step's accepted path in place and verifies its own tree in one
+    # call, and reads its outputs o back.  Uploads, compute and read-backs run on
+    # three streams with rotating buffer sets, so step k + 1's upload overlaps
     # step k's compute and step k - 1's read-back.
     h = gb.upload(tb, pin=True)
     in_keys = ["q", "k", "v", "g", "beta", "node_offsets", "parent", "path_offsets", "path_idx"]
     h2d = sum(h[k].numel() * h[k].element_size() for k in in_keys)
     d2h = o.numel() * o.element_size()
-    # the fused step still reads the previous step's tree (its accepted path),
-    # so it cycles three input sets instead of two
-    nset = 3 if args.fused else 2
+    # a step commits the previous step's accepted path (its tree's rows are still
+    # read), so the inputs cycle through three buffer sets
+    nset = 3
     bufs = [{k: torch.empty_like(d[k]) for k in in_keys} for _ in range(nset)]
     obufs = [torch.empty_like(o) for _ in range(2)]
     o_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
@@ -366,20 +379,12 @@ def run_ours(args, rank, world, local_rank):
         bj = bufs[j]
         gb.gdn_tree_build_desc(bj["parent"], bj["node_offsets"], tb.max_nodes, mask, depth, words,
                                status, stream)
-        if args.fused:
-            # commit the previous step's accepted path, then verify this step's tree
-            bp = bufs[(it - 1) % nset] if it > 0 else bj
-            gb.gdn_tree_commit_verify(bp, state, tb.max_nodes, tb.max_depth_bound, bj["q"], bj["k"],
-                                      bj["v"], bj["g"], bj["beta"], bj["node_offsets"], bj["parent"],
-                                      mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                                      S_new=state, out=obufs[jo], dev_status=status, stream=stream)
-        else:
-            gb.gdn_tree_verify(bj["q"], bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
-                               bj["parent"], mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
-                               out=obufs[jo], dev_status=status, stream=stream)
-            gb.gdn_tree_commit(bj["k"], bj["v"], bj["g"], bj["beta"], state, bj["node_offsets"],
-                               bj["parent"], bj["path_offsets"], bj["path_idx"], tb.max_nodes,
-                               max_path=tb.max_depth_bound, out=state, dev_status=status, stream=stream)
+        # commit the previous step's accepted path in place, then verify this step's tree
+        bp = bufs[(it - 1) % nset] if it > 0 else bj
+        gb.gdn_tree_commit_verify(bp, state, tb.max_nodes, tb.max_depth_bound, bj["q"], bj["k"],
+                                  bj["v"], bj["g"], bj["beta"], bj["node_offsets"], bj["parent"],
+                                  mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound,
+                                  S_new=state, out=obufs[jo], dev_status=status, stream=stream)
         ev_done[it].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[it])
@@ -394,10 +399,10 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     hbm_gbs, bf16_tf, peak_kind = load_peaks()
-    vbytes = fused_bytes(tb) if args.fused else verify_bytes(tb)
+    vbytes = verify_bytes(tb)
     v_s = statistics.mean(verify_ms) / 1e3
     achieved = vbytes / v_s / 1e9
-    kernel = "verify_tc_fused" if args.fused else dominant_kernel(tb)
+    kernel = dominant_kernel(tb)
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
@@ -415,8 +420,7 @@ def run_ours(args, rank, world, local_rank):
                    "tree": "random parent over nodes of depth < 16 (depth <= 16)",
                    "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
                    "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
-                   "step": ("build_desc + commit_verify (the previous accepted path committed, "
-                            "fused with the verification)") if args.fused else "build_desc + verify + commit",
+                   "step": "build_desc + verify + commit",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
@@ -426,16 +430,23 @@ def run_ours(args, rank, world, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "verify_only": {"us_per_launch": v_s * 1e6, "node_tokens_per_s": T / v_s,
                         "tflops": verify_flops(tb) / v_s / 1e12},
-        "step_bytes": ({"desc": desc_bytes(tb), "commit_verify": vbytes} if args.fused else
-                       {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)}),
+        "step_bytes": {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)},
+        "serving_order": {
+            "step": ("build_desc + gdn_tree_commit_verify: the accepted path committed, then the "
+                     "tree verified from the committed state, the verify launched as the commit's "
+                     "programmatic dependent"),
+            "ms_per_step": serving_s * 1e3 / args.steps,
+            "node_tokens_per_s": job_throughput(T, args.steps, serving_s, world),
+            "gpu_launches_per_step": 3},
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "pipeline": "serving loop: state resident and committed in place; per step "
-                            "q/k/v/g/beta + tree uploaded from pinned memory and o read back; "
-                            "upload, compute and read-back on three streams, two buffer sets"},
-        "gpu_launches": (2 if args.fused else 3) * args.steps,
+                "pipeline": "serving loop: state resident; per step q/k/v/g/beta + tree + path "
+                            "uploaded from pinned memory, the previous step's accepted path "
+                            "committed in place and the new tree verified (gdn_tree_commit_verify), "
+                            "o read back; upload, compute and read-back on three streams"},
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
 
@@ -680,8 +691,6 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
-    ap.add_argument("--fused", action="store_true",
-                    help="step = build_desc + gdn_tree_commit_verify (commit fused into the verify)")
     ap.add_argument("--sweep", action="store_true",
                     help="time fused verify against the per-branch baseline over the sweep grid")
     ap.add_argument("--sweep-reps", type=int, default=10)

@@ -56,6 +56,32 @@ int check_verify(const gdn_verify_args *a) {
     return GDN_OK;
 }
 
+int check_commit(const gdn_commit_args *a) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "commit args are NULL");
+    int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
+    if (st) return st;
+    if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
+    if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
+    if (a->max_path < 0) return fail(GDN_ERR_INVALID_ARG, "max_path %d < 0", a->max_path);
+    if (a->batch == 0) return GDN_OK;
+    if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
+        !a->path_offsets || !a->path_idx || !a->S_new)
+        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
+    return GDN_OK;
+}
+
+cudaError_t launch_commit_any(const gdn_commit_args &a, cudaStream_t stream) {
+    return gdn::commit_tc_supported(a)     ? gdn::launch_commit_tc(a, stream)
+           : gdn::commit_fast_supported(a) ? gdn::launch_commit_fast(a, stream)
+                                           : gdn::launch_commit_simt(a, stream);
+}
+
+// the verification; after_commit: the preceding launch in the stream commits its state
+cudaError_t launch_verify_any(const gdn_verify_args &a, cudaStream_t stream, bool after_commit) {
+    return gdn::verify_tc_supported(a) ? gdn::launch_verify_tc(a, stream, after_commit)
+                                       : gdn::launch_verify_simt(a, stream);
+}
+
 }  // namespace
 
 namespace gdn {
@@ -171,9 +197,7 @@ int gdn_tree_verify(const gdn_verify_args *a, void *stream) {
     g_err[0] = 0;
     int st = check_verify(a);
     if (st || a->batch == 0) return st;
-    cudaError_t e = gdn::verify_tc_supported(*a)
-                        ? gdn::launch_verify_tc(*a, (cudaStream_t)stream)
-                        : gdn::launch_verify_simt(*a, (cudaStream_t)stream);
+    cudaError_t e = launch_verify_any(*a, (cudaStream_t)stream, false);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "verify launch");
 }
 
@@ -187,44 +211,29 @@ int gdn_tree_verify_branches(const gdn_verify_args *a, void *stream) {
 
 int gdn_tree_commit(const gdn_commit_args *a, void *stream) {
     g_err[0] = 0;
-    if (!a) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
-    int st = check_common(a->batch, a->n_k_heads, a->n_v_heads, a->d_k, a->d_v, a->max_nodes);
-    if (st) return st;
-    if (!valid_dtype(a->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", a->qkv_dtype);
-    if (a->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", a->total_nodes);
-    if (a->max_path < 0) return fail(GDN_ERR_INVALID_ARG, "max_path %d < 0", a->max_path);
-    if (a->batch == 0) return GDN_OK;
-    if (!a->node_offsets || !a->k || !a->v || !a->g || !a->beta || !a->S0 || !a->parent ||
-        !a->path_offsets || !a->path_idx || !a->S_new)
-        return fail(GDN_ERR_INVALID_ARG, "a required pointer is NULL");
-    cudaError_t e = gdn::commit_tc_supported(*a)     ? gdn::launch_commit_tc(*a, (cudaStream_t)stream)
-                    : gdn::commit_fast_supported(*a) ? gdn::launch_commit_fast(*a, (cudaStream_t)stream)
-                                                     : gdn::launch_commit_simt(*a, (cudaStream_t)stream);
+    int st = check_commit(a);
+    if (st || a->batch == 0) return st;
+    cudaError_t e = launch_commit_any(*a, (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit launch");
 }
 
 int gdn_tree_commit_verify(const gdn_commit_args *c, const gdn_verify_args *v, void *stream) {
     g_err[0] = 0;
-    if (!c) return fail(GDN_ERR_INVALID_ARG, "commit args are NULL");
-    int st = check_verify(v);
+    int st = check_commit(c);
     if (st) return st;
-    st = check_common(c->batch, c->n_k_heads, c->n_v_heads, c->d_k, c->d_v, c->max_nodes);
+    if (!v) return fail(GDN_ERR_INVALID_ARG, "verify args are NULL");
+    gdn_verify_args vv = *v;
+    vv.S0 = c->S_new;  // the new tree is verified from the committed state
+    st = check_verify(&vv);
     if (st) return st;
-    if (!valid_dtype(c->qkv_dtype)) return fail(GDN_ERR_UNSUPPORTED, "unknown dtype %d", c->qkv_dtype);
-    if (c->total_nodes < 0) return fail(GDN_ERR_INVALID_ARG, "total_nodes %d < 0", c->total_nodes);
-    if (c->max_path < 0) return fail(GDN_ERR_INVALID_ARG, "max_path %d < 0", c->max_path);
-    if (c->batch != v->batch || c->n_k_heads != v->n_k_heads || c->n_v_heads != v->n_v_heads)
+    if (c->batch != v->batch || c->n_k_heads != v->n_k_heads || c->n_v_heads != v->n_v_heads ||
+        c->d_k != v->d_k || c->d_v != v->d_v)
         return fail(GDN_ERR_INVALID_ARG, "commit and verify shapes differ");
     if (v->batch == 0) return GDN_OK;
-    if (!c->node_offsets || !c->k || !c->v || !c->g || !c->beta || !c->S0 || !c->parent ||
-        !c->path_offsets || !c->path_idx || !c->S_new)
-        return fail(GDN_ERR_INVALID_ARG, "a required commit pointer is NULL");
-    if (!gdn::commit_verify_tc_supported(*c, *v))
-        return fail(GDN_ERR_UNSUPPORTED,
-                    "commit_verify: bf16 tokens, d = 128, max_nodes <= 128, max_depth and max_path in [1, 16], "
-                    "16-byte aligned tensors only");
-    cudaError_t e = gdn::launch_commit_verify_tc(*c, *v, (cudaStream_t)stream);
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "commit_verify launch");
+    cudaError_t e = launch_commit_any(*c, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    e = launch_verify_any(vv, (cudaStream_t)stream, true);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "verify launch");
 }
 
 int gdn_tree_states(const gdn_states_args *a, void *stream) {

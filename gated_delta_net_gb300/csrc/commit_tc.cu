@@ -120,6 +120,9 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
         if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
         return;
     }
+    // a verification launched as this grid's programmatic dependent may take the
+    // SMs as this grid's blocks finish (it waits for this grid before reading state)
+    griddep_launch_dependents();
     if ((int)blockIdx.x >= p.items) return;
     const int row = quad * 32 + lane, half = warp >> 2;  // tensor-memory lane = state row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;

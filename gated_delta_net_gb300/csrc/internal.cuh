@@ -84,13 +84,9 @@ cudaError_t ensure_smem(Kernel kern, int bytes, int (&have)[16]) {
     return e;
 }
 
-// tcgen05/TMA fast path; returns cudaErrorNotSupported when the shape is not covered
+// tcgen05/TMA fast path; after_commit launches it as the programmatic dependent
+// of the commit launched just before it in the stream
 bool verify_tc_supported(const gdn_verify_args &a);
-cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream);
-
-// the same kernel committing each item's state along the previous tree's
-// accepted path first and verifying the new tree from the committed state
-bool commit_verify_tc_supported(const gdn_commit_args &c, const gdn_verify_args &a);
-cudaError_t launch_commit_verify_tc(const gdn_commit_args &c, const gdn_verify_args &a, cudaStream_t stream);
+cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream, bool after_commit);
 
 }  // namespace gdn

@@ -61,6 +61,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the preceding grid has completed and its memory is visible (returns
+// at once when this grid was launched without a programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let a grid launched as this one's programmatic dependent be scheduled.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // proxies and fences
 // ---------------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async

@@ -25,8 +25,6 @@
 //   warps 0-3 ("tree"):  node metadata, paths, gamma; scatter of the Gram into
 //                        per-node ancestor rows (X and Y); X scaling; P; P rows.
 //   warps 4-7 ("state"): S0 conversion; right-hand side R rows; epilogue.
-//                        (In the fused kernel they also commit the state and
-//                        scatter Y, whose rows hold the path keys meanwhile.)
 //   thread 128 issues the TMA copies and the S0 and output MMAs, thread 0 the Gram.
 // The grid is persistent (two blocks per SM); a block walks its (request, value
 // head) items.  The next item's tree metadata is built during the current
@@ -37,6 +35,9 @@
 // A node whose right-hand side row turns non-finite has that row replaced by
 // zero in the output product and its subtree's outputs set to NaN, so
 // non-finite values never leave their own branch.
+// Launched as the dependent of a commit that writes the state (programmatic
+// dependent launch), the kernel starts on the SMs the commit frees: only the
+// state warps' first state read waits for the commit grid to finish.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -69,11 +70,6 @@ constexpr int OFF_MISC = OFF_I + 2 * kN * 4;            // tmem slot, poisoned-n
 constexpr int OFF_BAR = OFF_MISC + 64;
 constexpr int kBars = 12;
 constexpr int kSmemBytes = OFF_BAR + kBars * 8;
-// the fused commit-then-verify kernel adds: chain coefficients [16][16], path
-// gamma, e^gamma, decay to the end, beta [16] each, path node rows [16], errors[2]
-constexpr int OFF_CMT = kSmemBytes;
-constexpr int kSmemFused = OFF_CMT + (kMaxDepth * kMaxDepth + 4 * kMaxDepth + kMaxDepth + 2) * 4;
-static_assert(2 * (kSmemFused + 1024) <= 233472, "two fused blocks must fit in one SM's shared memory");
 
 // mbarrier indices
 enum { B_KQ, B_GRAM, B_DESC, B_TFREE, B_S0IN, B_S0, B_R, B_P, B_OUT, B_V, B_META, B_ZFREE };
@@ -86,13 +82,6 @@ struct TcParams {
     const float *g, *beta, *S0;
     void *o;
     int32_t *status;
-    // fused commit of the previous tree's accepted path (the state read is S0,
-    // the committed state S_new, which this kernel then verifies from)
-    int c_total;
-    const int32_t *c_offsets, *c_parent, *c_poff, *c_pidx;
-    const __nv_bfloat16 *c_k, *c_v;
-    const float *c_g, *c_beta;
-    float *S_new;
 };
 
 // one (request, value head) work item
@@ -164,9 +153,7 @@ __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// kFused: the state of each item is first committed along the previous tree's
-// accepted path (written to S_new), and the new tree is verified from it.
-template <typename Tout, bool kFused>
+template <typename Tout>
 __global__ void __launch_bounds__(kT, 2)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, TcParams p) {
@@ -188,12 +175,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const int row = quad * 32 + lane;  // tensor-memory lane of this thread = a tree node
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const bool issuer = tid == 128;
+    // a block that leaves early still waits for a preceding grid, so that this
+    // grid never completes before the grid it depends on
     if ((smem_u32(sm) & 1023u) != 0u) {
         if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
+        griddep_wait();
         return;
     }
     Item cur;
-    if (!find_item(p, blockIdx.x, gridDim.x, tid == 0, cur)) return;
+    if (!find_item(p, blockIdx.x, gridDim.x, tid == 0, cur)) {
+        griddep_wait();
+        return;
+    }
 
     // ---- set-up, once per block ---------------------------------------------
     if (tid == 0) {
@@ -251,10 +244,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         // raw ancestor rows start at zero (entries past a node's depth stay zero)
         reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4 *>(Xs + i * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
-        if (!kFused) {  // the fused kernel's state warps clear Y after using it for path keys
-            reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
-            reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(Ys + i * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
         if (i < 4) pset[pp * 4 + i] = 0u;
         if (i == 0) s_err[pp] = 0;
         named_sync(1, 128);
@@ -355,179 +346,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         mbar_arrive(&bar[B_S0IN]);
     };
 
-    // Fused kernel, state warps: the commit of the previous tree's accepted path
-    // p_1..p_L for this item's (request, value head), one state row r per thread,
-    // in fp32:
-    //     W_t = S_r . k_t,   u_t = beta_t (v_t[r] - e^gamma_t W_t) - sum_{s<t} c_ts u_s,
-    //     S_new_r = e^gamma_L S_r + sum_t e^(gamma_L - gamma_t) u_t k_t
-    // with c_ts = beta_t e^(gamma_t - gamma_s) (k_t . k_s); the rows go to S_new
-    // (fp32) and, as bf16, into the S0 space for this item's S0 MMAs.  The path
-    // keys sit in the raw-Y rows until the Y scatter, which needs them zeroed.
-    // A path that is not root-first along parent -> child edges sets
-    // GDN_DEV_BAD_PATH: that item's S_new and outputs are left unwritten.
-    auto commit_s0 = [&](const Item &it, int pp) {
-        float *coef = reinterpret_cast<float *>(sm + OFF_CMT);
-        float *cgam = coef + kMaxDepth * kMaxDepth, *cegam = cgam + kMaxDepth, *cfdec = cegam + kMaxDepth,
-              *cbet = cfdec + kMaxDepth;
-        int *cnode = reinterpret_cast<int *>(cbet + kMaxDepth), *c_err = cnode + kMaxDepth;
-        const uint32_t *keyw = reinterpret_cast<const uint32_t *>(Ys);  // [16][128] bf16 as pairs
-        const int st = tid - 128;                                       // the state row
-        const int clo = __ldg(p.c_offsets + it.b), cn = __ldg(p.c_offsets + it.b + 1) - clo;
-        const int pa = __ldg(p.c_poff + it.b), L = __ldg(p.c_poff + it.b + 1) - pa;
-        const bool shape_ok = L >= 0 && L <= kMaxDepth && L <= cn && clo >= 0 && clo + cn <= p.c_total;
-        if (st == 0) c_err[pp] = shape_ok ? 0 : (L > kMaxDepth && L <= cn ? GDN_DEV_TOO_DEEP : GDN_DEV_BAD_PATH);
-        named_sync(2, 128);
-        if (shape_ok && st < L) {
-            const int node = __ldg(p.c_pidx + pa + st);
-            const int expect = st == 0 ? -1 : __ldg(p.c_pidx + pa + st - 1);
-            const bool in = node >= 0 && node < cn;
-            if (!in || __ldg(p.c_parent + clo + node) != expect) atomicOr(&c_err[pp], GDN_DEV_BAD_PATH);
-            const int64_t grow = clo + (in ? node : 0);
-            cnode[st] = (int)grow;
-            cgam[st] = __ldg(p.c_g + grow * p.hv_n + it.hv);
-            cbet[st] = __ldg(p.c_beta + grow * p.hv_n + it.hv);
-        }
-        named_sync(2, 128);
-        const int err = c_err[pp];
-        const int Lc = err ? 0 : L;  // a malformed path commits nothing (and nothing is stored)
-        // path keys: 16 rows x 16 pieces of 16 bytes, rows past Lc zero
-        for (int e = st; e < kMaxDepth * 16; e += 128) {
-            const int t = e >> 4, c = e & 15;
-            uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-            if (t < Lc) kv = __ldg(reinterpret_cast<const uint4 *>(p.c_k + ((int64_t)cnode[t] * p.hk_n + it.hk) * kD) + c);
-            reinterpret_cast<uint4 *>(Ys)[e] = kv;
-        }
-        if (st == 0) {
-            if (err) flag(p.status, err);
-            float acc = 0.f;
-            for (int t = 0; t < Lc; ++t) {
-                acc += cgam[t];
-                cgam[t] = acc;
-                cegam[t] = expf(acc);
-            }
-            for (int t = 0; t < Lc; ++t) cfdec[t] = expf(acc - cgam[t]);
-        }
-        named_sync(2, 128);
-        // chain coefficients: one state warp per pair (t, s), s < t
-        for (int pr = sw; pr < Lc * (Lc - 1) / 2; pr += 4) {
-            int t = 1, base = 0;
-            while (base + t <= pr) { base += t; ++t; }
-            const int s_ = pr - base;
-            const uint32_t a0 = keyw[t * 64 + lane * 2], a1 = keyw[t * 64 + lane * 2 + 1];
-            const uint32_t b0 = keyw[s_ * 64 + lane * 2], b1 = keyw[s_ * 64 + lane * 2 + 1];
-            float d = bf16_lo(a0) * bf16_lo(b0);
-            d = fmaf(bf16_hi(a0), bf16_hi(b0), d);
-            d = fmaf(bf16_lo(a1), bf16_lo(b1), d);
-            d = fmaf(bf16_hi(a1), bf16_hi(b1), d);
-            d = warp_sum(d);
-            if (lane == 0) coef[t * kMaxDepth + s_] = cbet[t] * expf(cgam[t] - cgam[s_]) * d;
-        }
-        named_sync(2, 128);
-        // this thread's row: W_t over 16-column chunks (keys read as broadcasts);
-        // the t loops stop at the path length (uniform over the block) and the
-        // next chunk of the row is loaded while this one is used
-        const float *srow = p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD) + (int64_t)st * kD;
-        auto load_chunk = [&](int c0, float4 (&f)[4]) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) f[q] = __ldg(reinterpret_cast<const float4 *>(srow + c0) + q);
-        };
-        auto unpack = [](const float4 (&f)[4], float (&x)[16]) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                x[q * 4 + 0] = f[q].x; x[q * 4 + 1] = f[q].y; x[q * 4 + 2] = f[q].z; x[q * 4 + 3] = f[q].w;
-            }
-        };
-        float W[kMaxDepth];
-#pragma unroll
-        for (int t = 0; t < kMaxDepth; ++t) W[t] = 0.f;
-        float4 nxt[4];
-        load_chunk(0, nxt);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            float x[16];
-            unpack(nxt, x);
-            if (c0 + 16 < kD) load_chunk(c0 + 16, nxt);
-#pragma unroll
-            for (int t = 0; t < kMaxDepth; ++t) {
-                if (t < Lc) {
-                    const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
-                    const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
-                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                    float w = W[t];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        w = fmaf(x[2 * e], bf16_lo(kw[e]), w);
-                        w = fmaf(x[2 * e + 1], bf16_hi(kw[e]), w);
-                    }
-                    W[t] = w;
-                }
-            }
-        }
-        // the second pass re-reads the row from the start
-        load_chunk(0, nxt);
-        // the chain for this row, then A_t = e^(gamma_L - gamma_t) u_t
-        float A[kMaxDepth];
-        {
-            const __nv_bfloat16 *vcol = p.c_v + (int64_t)it.hv * kD + st;
-            float vt[kMaxDepth];
-#pragma unroll
-            for (int t = 0; t < kMaxDepth; ++t)
-                vt[t] = t < Lc ? __bfloat162float(vcol[(int64_t)cnode[t] * p.hv_n * kD]) : 0.f;
-#pragma unroll
-            for (int t = 0; t < kMaxDepth; ++t) {
-                float u = 0.f;
-                if (t < Lc) {
-                    u = cbet[t] * (vt[t] - cegam[t] * W[t]);
-#pragma unroll
-                    for (int s2 = 0; s2 < t; ++s2) u = fmaf(-coef[t * kMaxDepth + s2], A[s2], u);
-                }
-                A[t] = u;
-            }
-#pragma unroll
-            for (int t = 0; t < kMaxDepth; ++t) A[t] = t < Lc ? A[t] * cfdec[t] : 0.f;
-        }
-        const float eL = Lc > 0 ? cegam[Lc - 1] : 1.f;
-        float *drow = p.S_new + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD) + (int64_t)st * kD;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            float x[16];
-            unpack(nxt, x);
-            if (c0 + 16 < kD) load_chunk(c0 + 16, nxt);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] *= eL;
-#pragma unroll
-            for (int t = 0; t < kMaxDepth; ++t) {
-                if (t < Lc) {
-                    const uint4 ka = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[0];
-                    const uint4 kb = reinterpret_cast<const uint4 *>(keyw + t * 64 + c0 / 2)[1];
-                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        x[2 * e] = fmaf(A[t], bf16_lo(kw[e]), x[2 * e]);
-                        x[2 * e + 1] = fmaf(A[t], bf16_hi(kw[e]), x[2 * e + 1]);
-                    }
-                }
-            }
-            if (!err) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    reinterpret_cast<float4 *>(drow + c0)[q] = make_float4(x[q * 4 + 0], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
-            }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-                *reinterpret_cast<uint4 *>(sm + OFF_S0 + sw128_offset(st, c0 + h2 * 8)) =
-                    make_uint4(pack_bf16(x[h2 * 8 + 0], x[h2 * 8 + 1]), pack_bf16(x[h2 * 8 + 2], x[h2 * 8 + 3]),
-                               pack_bf16(x[h2 * 8 + 4], x[h2 * 8 + 5]), pack_bf16(x[h2 * 8 + 6], x[h2 * 8 + 7]));
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar[B_S0IN]);
-        // the raw-Y rows back to zero for the Y scatter (every key has been read)
-        named_sync(2, 128);
-        reinterpret_cast<uint4 *>(Ys + st * kMaxDepth)[0] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4 *>(Ys + st * kMaxDepth)[1] = make_uint4(0u, 0u, 0u, 0u);
-        named_sync(2, 128);
-    };
-
     // scatter of one half of the Gram: lane a holds k_a.k_i (cols 0..127) or
     // k_a.q_i (cols 128..255) and writes them into the ancestor rows of its
     // descendants i (the descendant bits of a come from its mask row).
@@ -550,9 +368,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
     // ---- the first item's operands -------------------------------------------
     if (issuer) issue_kq(cur);
-    if (tree) tree_meta(cur, 0);
-    else if constexpr (kFused) commit_s0(cur, 0);
-    else state_s0(cur);
+    if (tree) {
+        tree_meta(cur, 0);
+    } else {
+        griddep_wait();  // S0 may be the output of the preceding grid (a commit)
+        state_s0(cur);
+    }
 
     const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
     for (int it = 0;; ++it) {
@@ -608,7 +429,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             ok = mbar_wait(&bar[B_GRAM], ph) && ok;
             tc_fence_after();
             scatter(0, Xs, true);
-            if constexpr (!kFused) scatter(128, Ys, false);
+            scatter(128, Ys, false);
             tc_fence_before();
             mbar_arrive(&bar[B_TFREE]);
 
@@ -673,15 +494,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             cur = nx;
         } else {
             // ===================== state warps =================================
-            // (fused kernel) full part of the Gram -> raw Y rows
             ok = mbar_wait(&bar[B_DESC], ph) && ok;
-            if constexpr (kFused) {
-                ok = mbar_wait(&bar[B_GRAM], ph) && ok;
-                tc_fence_after();
-                scatter(128, Ys, false);
-                tc_fence_before();
-            }
-            mbar_arrive(&bar[B_TFREE]);
+            mbar_arrive(&bar[B_TFREE]);  // the tree warps read the Gram out
 
             if (issuer) {
                 // S0 part: W = K S0^T (cols 0..127), Z = Q S0^T (cols 128..255)
@@ -712,8 +526,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             uint32_t desc_row[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) desc_row[w] = msk[j * 4 + w];
-            bool item_good = s_err[ph] == 0;
-            if constexpr (kFused) item_good = item_good && reinterpret_cast<const int *>(sm + OFF_CMT)[kMaxDepth * kMaxDepth + 5 * kMaxDepth + ph] == 0;
+            const bool item_good = s_err[ph] == 0;
             const bool store = item_good && j < n;
             mbar_arrive(&bar[B_META]);
 
@@ -852,8 +665,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 named_sync(2, 128);  // the S0 space may be written again
             }
             if (!more) break;
-            if constexpr (kFused) commit_s0(nx, ph ^ 1);
-            else state_s0(nx);
+            state_s0(nx);
             cur = nx;
         }
     }
@@ -887,10 +699,7 @@ bool verify_tc_supported(const gdn_verify_args &a) {
            aligned16(a.k) && aligned16(a.v) && aligned16(a.S0) && aligned16(a.o) && tensor_map_encoder() != nullptr;
 }
 
-namespace {
-
-template <bool kFused>
-cudaError_t launch_tc(const gdn_verify_args &a, const gdn_commit_args *c, cudaStream_t stream) {
+cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream, bool after_commit) {
     CUtensorMap tmK, tmQ, tmV, tmO;
     if (!encode_tokens(&tmK, a.k, a.n_k_heads, a.total_nodes) ||
         !encode_tokens(&tmQ, a.q, a.n_k_heads, a.total_nodes) ||
@@ -902,51 +711,32 @@ cudaError_t launch_tc(const gdn_verify_args &a, const gdn_commit_args *c, cudaSt
     } else {
         tmO = tmV;  // unused by the fp32-output kernel
     }
-    TcParams p = {};
+    TcParams p;
     p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.words = a.mask_words < 4 ? a.mask_words : 4;
     p.total = a.total_nodes; p.items = a.batch * a.n_v_heads; p.scale = a.scale;
     p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth; p.mask = a.anc_mask;
-    p.g = a.g; p.beta = a.beta; p.S0 = kFused ? c->S0 : a.S0;
+    p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
     p.o = a.o; p.status = a.dev_status;
-    if (kFused) {
-        p.c_total = c->total_nodes; p.c_offsets = c->node_offsets; p.c_parent = c->parent;
-        p.c_poff = c->path_offsets; p.c_pidx = c->path_idx;
-        p.c_k = static_cast<const __nv_bfloat16 *>(c->k); p.c_v = static_cast<const __nv_bfloat16 *>(c->v);
-        p.c_g = c->g; p.c_beta = c->beta; p.S_new = c->S_new;
-    }
-    constexpr int smem = kFused ? kSmemFused : kSmemBytes;
+    static int have_bf16[16], have_f32[16];
+    auto kern = a.out_dtype == GDN_BF16 ? verify_tc_kernel<__nv_bfloat16> : verify_tc_kernel<float>;
+    cudaError_t e = ensure_smem(kern, kSmemBytes, a.out_dtype == GDN_BF16 ? have_bf16 : have_f32);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
     // persistent: two blocks per SM (tensor memory and shared memory allow two)
-    const dim3 grid((unsigned)std::min(p.items, 2 * sm_count()));
-    cudaError_t e;
-    if (a.out_dtype == GDN_BF16) {
-        static int have[16];
-        e = ensure_smem(verify_tc_kernel<__nv_bfloat16, kFused>, smem, have);
-        if (e != cudaSuccess) return e;
-        verify_tc_kernel<__nv_bfloat16, kFused><<<grid, kT, smem, stream>>>(tmK, tmQ, tmV, tmO, p);
-    } else {
-        static int have[16];
-        e = ensure_smem(verify_tc_kernel<float, kFused>, smem, have);
-        if (e != cudaSuccess) return e;
-        verify_tc_kernel<float, kFused><<<grid, kT, smem, stream>>>(tmK, tmQ, tmV, tmO, p);
-    }
-    return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream) {
-    return launch_tc<false>(a, nullptr, stream);
-}
-
-bool commit_verify_tc_supported(const gdn_commit_args &c, const gdn_verify_args &a) {
-    return verify_tc_supported(a) && c.qkv_dtype == GDN_BF16 && c.d_k == kD && c.d_v == kD &&
-           c.batch == a.batch && c.n_k_heads == a.n_k_heads && c.n_v_heads == a.n_v_heads &&
-           c.max_path >= 1 && c.max_path <= kMaxDepth && aligned16(c.k) && aligned16(c.S0) &&
-           aligned16(c.S_new);
-}
-
-cudaError_t launch_commit_verify_tc(const gdn_commit_args &c, const gdn_verify_args &a, cudaStream_t stream) {
-    return launch_tc<true>(a, &c, stream);
+    cfg.gridDim = dim3((unsigned)std::min(p.items, 2 * sm_count()));
+    cfg.blockDim = dim3(kT);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    // after a commit of the state in the same stream, the launch may begin while
+    // the commit drains (programmatic dependent launch; the kernel waits for it
+    // before its first state read)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = after_commit ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmK, tmQ, tmV, tmO, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace gdn

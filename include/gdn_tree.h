@@ -236,22 +236,22 @@ typedef struct {
 GDN_API int gdn_tree_commit(const gdn_commit_args *args, void *stream);
 
 /*
- * gdn_tree_commit_verify -- the delayed commit and the next verification in
- * one pass (same section, Solution bullet 4: the state is committed in the
- * next decoding iteration).  For every (request, value head) the state
- * commit->S0 is committed along the previous tree's accepted path (commit's
- * tree, tokens and path) and written to commit->S_new, and the new tree
- * (verify's) is verified from that committed state, which is never read back
- * from memory: one state read per (request, head) instead of two.
- *   verify->S0 is not read.  commit->S_new may equal commit->S0 (in place).
- *   Both calls' shapes must agree (batch, heads, d_k = d_v = 128, bf16
- *   tokens); the verify side needs max_nodes <= 128 and 1 <= max_depth <= 16,
- *   the commit side 1 <= max_path <= 16 (else GDN_ERR_UNSUPPORTED: run
- *   gdn_tree_commit, then gdn_tree_verify).
- *   Results equal those two calls: the commit in fp32 (1e-4 of max|S|), the
- *   verification from the committed state rounded to bf16 like the fast path
- *   of gdn_tree_verify.  A bad path sets GDN_DEV_BAD_PATH (GDN_DEV_TOO_DEEP
- *   past 16 nodes): that request's S_new and outputs are left unwritten.
+ * gdn_tree_commit_verify -- the delayed commit followed by the next
+ * verification (same section, Solution bullet 4: the state is committed in the
+ * next decoding iteration).  commit->S0 is committed along the previous tree's
+ * accepted path (commit's tree, tokens and path) into commit->S_new, and the
+ * new tree (verify's) is verified from commit->S_new; verify->S0 is not read.
+ *   Results equal gdn_tree_commit then gdn_tree_verify on the same stream.
+ *   The two launches overlap: the verification is launched as the commit's
+ *   programmatic dependent, its blocks start on the SMs the commit releases,
+ *   and each waits for the whole commit before its first state read.
+ *   commit->S_new may equal commit->S0 (in place); it must not overlap any
+ *   other input of the verification.  Shapes of both calls must agree (batch,
+ *   heads, d_k, d_v); any shapes that both gdn_tree_commit and
+ *   gdn_tree_verify accept are accepted.
+ *   A bad path sets GDN_DEV_BAD_PATH (GDN_DEV_TOO_DEEP past the commit kernel's
+ *   limit) and leaves that request's S_new unwritten; its new outputs are then
+ *   computed from whatever S_new held and must be discarded.
  */
 GDN_API int gdn_tree_commit_verify(const gdn_commit_args *commit, const gdn_verify_args *verify,
                                    void *stream);

@@ -1,11 +1,12 @@
 """GPU parity of gdn_tree_commit_verify: the delayed commit of the previous
-tree's accepted path fused with the verification of the next tree ("Trees from
-Marginals", gist.science Technical Summary, section 3, Solution, bullet 4: the
-state is committed in the next decoding iteration).
+tree's accepted path followed by the verification of the next tree from the
+committed state, the verification launched as the commit's programmatic
+dependent ("Trees from Marginals", gist.science Technical Summary, section 3,
+Solution, bullet 4: the state is committed in the next decoding iteration).
 
 Reference: oracle.commit on the previous tree (the committed state, fp32
 tolerance 1e-4 * max|S|), then oracle.verify of the new tree from that state
-(bf16 tolerance 2e-2 * max|o|).
+(bf16 tolerance 2e-2 * max|o|; fp32 1e-4 relative).
 """
 import numpy as np
 import pytest
@@ -87,6 +88,53 @@ def test_empty_previous_path_keeps_the_state_exactly():
     assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
 
 
+def test_general_shapes_chain_the_general_kernels():
+    # fp32 tokens, d = 16, a deep chain: neither tensor-core kernel applies
+    parents = [np.arange(-1, 39, dtype=np.int32), W.depth_capped_random_tree(np.random.default_rng(5), 30, 40)]
+    prev = W.custom(29, parents, n_k_heads=2, n_v_heads=4, d=16, qkv_dtype="f32")
+    new = W.custom(30, parents, n_k_heads=2, n_v_heads=4, d=16, qkv_dtype="f32")
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes, dev_status=status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 0, dn["q"], dn["k"], dn["v"], dn["g"],
+                                     dn["beta"], dn["node_offsets"], dn["parent"], mask, depth,
+                                     new.max_nodes, max_depth=0, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_STATE
+
+
+def test_replays_in_a_cuda_graph():
+    prev, new = W.serving_target(seed=31, batch=4), W.serving_target(seed=32, batch=4)
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes, dev_status=status)
+    S_new = torch.empty_like(dp["S0"])
+    o = torch.empty((new.total_nodes, new.n_v_heads, new.d_v), dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 16, dn["q"], dn["k"], dn["v"], dn["g"],
+                                  dn["beta"], dn["node_offsets"], dn["parent"], mask, depth, new.max_nodes,
+                                  S_new=S_new, out=o, dev_status=status, stream=torch.cuda.current_stream())
+
+    call()
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    o_eager, S_eager = o.clone(), S_new.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(3):
+        o.zero_()
+        S_new.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        gb.check_status(status)
+        assert torch.equal(o, o_eager) and torch.equal(S_new, S_eager)
+
+
 def test_bad_previous_path_is_flagged_and_left_unwritten():
     parent = W.depth_capped_random_tree(np.random.default_rng(3), 30, 16)
     parents = [parent, parent, parent]
@@ -105,7 +153,7 @@ def test_bad_previous_path_is_flagged_and_left_unwritten():
                               dn["node_offsets"], dn["parent"], mask, depth, 30, S_new=sentinel,
                               out=o_init, dev_status=status)
     torch.cuda.synchronize()
-    assert int(status.item()) == 2
-    assert torch.all(sentinel[1] == 3.0)
-    assert torch.all(o_init[30:60] == 5.0)
-    assert not torch.all(sentinel[0] == 3.0) and not torch.all(o_init[:30] == 5.0)
+    assert int(status.item()) == 2                   # GDN_DEV_BAD_PATH
+    assert torch.all(sentinel[1] == 3.0)             # the bad request's state is not committed
+    assert not torch.all(sentinel[0] == 3.0) and not torch.all(sentinel[2] == 3.0)
+    assert not torch.all(o_init[:30] == 5.0)
