@@ -93,6 +93,34 @@ def test_commit_rejects_bad_arguments(L):
     assert L.gdn_tree_commit(None, None) == binding.GDN_ERR_INVALID_ARG
 
 
+def test_commit_verify_rejects_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    cbase = dict(batch=1, n_k_heads=1, n_v_heads=1, d_k=16, d_v=16, total_nodes=12, max_nodes=12,
+                 max_path=0, qkv_dtype=0,
+                 node_offsets=fake, k=fake, v=fake, g=fake, beta=fake, S0=fake, parent=fake,
+                 path_offsets=fake, path_idx=fake, S_new=fake, dev_status=fake)
+    f = L.gdn_tree_commit_verify
+    v = _verify_args(S0=None)  # the verify side's S0 is not read: the committed state is
+    for ckw, vkw, code in ((dict(S_new=None), {}, binding.GDN_ERR_INVALID_ARG),
+                           ({}, dict(q=None), binding.GDN_ERR_INVALID_ARG),
+                           (dict(n_v_heads=2), dict(n_v_heads=1), binding.GDN_ERR_INVALID_ARG),
+                           (dict(batch=2), {}, binding.GDN_ERR_INVALID_ARG),
+                           (dict(d_k=32, d_v=32), {}, binding.GDN_ERR_INVALID_ARG),
+                           (dict(d_k=8), {}, binding.GDN_ERR_UNSUPPORTED),
+                           ({}, dict(d_v=48), binding.GDN_ERR_UNSUPPORTED),
+                           (dict(max_path=-1), {}, binding.GDN_ERR_INVALID_ARG)):
+        c = binding.CommitArgs(**{**cbase, **ckw})
+        vv = _verify_args(S0=None, **vkw)
+        assert f(ctypes.byref(c), ctypes.byref(vv), None) == code, (ckw, vkw)
+        assert L.gdn_last_error().decode() != ""
+    c = binding.CommitArgs(**cbase)
+    assert f(None, ctypes.byref(v), None) == binding.GDN_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), None, None) == binding.GDN_ERR_INVALID_ARG
+    c0 = binding.CommitArgs(**{**cbase, "batch": 0})
+    v0 = _verify_args(batch=0, S0=None, q=None)
+    assert f(ctypes.byref(c0), ctypes.byref(v0), None) == binding.GDN_OK
+
+
 def test_build_desc_rejects_bad_arguments(L):
     fake = ctypes.c_void_p(0x1000)
     f = L.gdn_tree_build_desc
