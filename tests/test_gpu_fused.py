@@ -106,6 +106,24 @@ def test_general_shapes_chain_the_general_kernels():
     assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_STATE
 
 
+def test_tensor_core_verify_after_the_general_commit():
+    # max_path = 0 (unknown) sends the commit to the general kernel, which never
+    # signals its dependents early; the tensor-core verify is still launched as its
+    # programmatic dependent and must still see the whole committed state
+    prev, new = W.serving_target(seed=33, batch=5), W.serving_target(seed=34, batch=5)
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes, dev_status=status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 0, dn["q"], dn["k"], dn["v"], dn["g"],
+                                     dn["beta"], dn["node_offsets"], dn["parent"], mask, depth,
+                                     new.max_nodes, max_depth=16, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
 def test_replays_in_a_cuda_graph():
     prev, new = W.serving_target(seed=31, batch=4), W.serving_target(seed=32, batch=4)
     dp, dn = gb.upload(prev), gb.upload(new)
