@@ -396,6 +396,24 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = reduce_max(t_start.elapsed_time(t_end) / 1e3, dev)
     e2e_value = job_throughput(T, e2e_steps, e2e_s, world)
 
+    # the host link's own bound for this loop: the same uploads and read-backs
+    # as plain copies on the same streams, no compute
+    torch.cuda.synchronize()
+    c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c_start.record(up)
+    down.wait_event(c_start)
+    for it in range(e2e_steps):
+        j, jo = it % nset, it % 2
+        with torch.cuda.stream(up):
+            for k in in_keys:
+                bufs[j][k].copy_(h[k], non_blocking=True)
+        with torch.cuda.stream(down):
+            o_h[jo].copy_(obufs[jo], non_blocking=True)
+    down.wait_stream(up)
+    c_end.record(down)
+    torch.cuda.synchronize()
+    copy_s = reduce_max(c_start.elapsed_time(c_end) / 1e3, dev)
+
     if rank != 0:
         return None
     hbm_gbs, bf16_tf, peak_kind = load_peaks()
@@ -442,6 +460,8 @@ def run_ours(args, rank, world, local_rank):
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copy_only_ms_per_step": copy_s * 1e3 / e2e_steps,
+                "frac_of_copy_bound": copy_s / e2e_s,
                 "pipeline": "serving loop: state resident; per step q/k/v/g/beta + tree + path "
                             "uploaded from pinned memory, the previous step's accepted path "
                             "committed in place and the new tree verified (gdn_tree_commit_verify), "
