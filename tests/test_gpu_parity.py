@@ -164,6 +164,43 @@ def test_verify_tree_sizes_sampled_against_oracle():
     assert rel_err(got, ref) <= TOL_BF16
 
 
+def test_commit_full_throughput_workload():
+    """The commit of the throughput workload (batch 64 x 32 value heads, every
+    request's accepted path) in the benchmark's launch configuration, every state
+    checked against the oracle."""
+    tb = W.serving_target()
+    S, status = run_commit(tb, max_path=tb.max_depth_bound)
+    gb.check_status(status)
+    ref, st = oracle.commit(tb)
+    assert st == 0
+    assert rel_err(S.cpu().numpy(), ref) <= TOL_STATE
+
+
+def test_commit_verify_full_throughput_workload_sampled():
+    """The serving-order call at full size: the previous tree's path committed,
+    the next tree verified from the committed state; every committed state and
+    sampled outputs checked against the oracle."""
+    prev, new = W.serving_target(seed=41), W.serving_target(seed=42)
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = run_desc(dn, new, status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, prev.max_depth_bound, dn["q"], dn["k"],
+                                     dn["v"], dn["g"], dn["beta"], dn["node_offsets"], dn["parent"], mask,
+                                     depth, new.max_nodes, max_depth=new.max_depth_bound, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S_ref, st = oracle.commit(prev)
+    assert st == 0
+    assert rel_err(S.cpu().numpy(), S_ref) <= TOL_STATE
+    new.S0 = S_ref
+    rng = np.random.default_rng(1)
+    sel = [(int(b), int(h), int(i)) for b in rng.choice(new.batch, 16, replace=False)
+           for h in rng.choice(new.n_v_heads, 4, replace=False) for i in rng.choice(128, 8, replace=False)]
+    ref = oracle.verify_selected(new, sel)
+    got = np.stack([o[new.node_offsets[b] + i, h].float().cpu().numpy() for b, h, i in sel])
+    assert rel_err(got, ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("n,batch", [(8, 8), (16, 1), (32, 8), (64, 8), (128, 8), (256, 1),
                                      (256, 8)])
 def test_sweep_points(n, batch):
