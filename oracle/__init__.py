@@ -49,19 +49,18 @@ def build(force: bool = False) -> str:
 
 def bind(lib):
     """Declare the C signatures on a loaded oracle library."""
-    if True:
-        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        P = ctypes.c_void_p
-        lib.gdn_oracle_build_desc.argtypes = [P, P, i32, i32, P, P]
-        lib.gdn_oracle_build_desc.restype = ctypes.c_int
-        lib.gdn_oracle_verify.argtypes = [i32] * 5 + [P] * 8 + [f64, P, i32]
-        lib.gdn_oracle_verify.restype = i32
-        lib.gdn_oracle_verify_sel.argtypes = [i32] * 5 + [P] * 8 + [f64, P, i64, P, i32]
-        lib.gdn_oracle_verify_sel.restype = i32
-        lib.gdn_oracle_commit.argtypes = [i32] * 5 + [P] * 9 + [P, i32]
-        lib.gdn_oracle_commit.restype = i32
-        lib.gdn_oracle_state_at.argtypes = [i32] * 5 + [P] * 7 + [i32, i32, i32, P]
-        lib.gdn_oracle_state_at.restype = i32
+    i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    P = ctypes.c_void_p
+    lib.gdn_oracle_build_desc.argtypes = [P, P, i32, i32, P, P]
+    lib.gdn_oracle_build_desc.restype = ctypes.c_int
+    lib.gdn_oracle_verify.argtypes = [i32] * 5 + [P] * 8 + [f64, P, i32]
+    lib.gdn_oracle_verify.restype = i32
+    lib.gdn_oracle_verify_sel.argtypes = [i32] * 5 + [P] * 8 + [f64, P, i64, P, i32]
+    lib.gdn_oracle_verify_sel.restype = i32
+    lib.gdn_oracle_commit.argtypes = [i32] * 5 + [P] * 9 + [P, i32]
+    lib.gdn_oracle_commit.restype = i32
+    lib.gdn_oracle_state_at.argtypes = [i32] * 5 + [P] * 7 + [i32, i32, i32, P]
+    lib.gdn_oracle_state_at.restype = i32
     return lib
 
 

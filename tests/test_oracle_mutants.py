@@ -19,6 +19,14 @@ MUTANTS = {
     "decay_sign": ("const double alpha = exp(P->g[t * P->Hv + h]);",
                    "const double alpha = exp(-P->g[t * P->Hv + h]);"),
     "drop_beta_in_erase": ("- beta * Sk[n] * kt[m]", "- Sk[n] * kt[m]"),
+    # the selected-output entry point: value head and node swapped, and the
+    # request's row offset dropped from its read-out row
+    "selected_swap_head_node": ("int32_t b = (int32_t)J->sel[3 * u], h = (int32_t)J->sel[3 * u + 1];\n"
+                                "            int32_t i = (int32_t)J->sel[3 * u + 2];",
+                                "int32_t b = (int32_t)J->sel[3 * u], h = (int32_t)J->sel[3 * u + 2];\n"
+                                "            int32_t i = (int32_t)J->sel[3 * u + 1];"),
+    "selected_drop_request_offset": ("readout(P, S, (int64_t)P->offsets[b] + i, h, J->out + u * P->dv);",
+                                     "readout(P, S, (int64_t)i, h, J->out + u * P->dv);"),
 }
 
 PIN_CASES = [
@@ -28,6 +36,8 @@ PIN_CASES = [
     lambda: pins.test_brute_force_all_forests(4),
     lambda: pins.test_head_sharing_equals_duplicated_key_heads(),
     lambda: pins.test_chain_matches_matrix_form(),
+    # every request has Hv nodes here, so a swapped (h, i) stays inside the arrays
+    lambda: pins.test_verify_selected_matches_verify("square"),
 ]
 
 

@@ -382,3 +382,50 @@ def test_descriptor_flags_bad_parent():
         _, _, st = oracle.build_desc(np.array(parent, np.int32),
                                      np.array([0, len(parent)], np.int32), 1)
         assert st == 1
+
+
+# ----------------------------------------------------------------------------
+# selected outputs (the checker of the full-size GPU tests and the CPU baseline)
+# ----------------------------------------------------------------------------
+
+def _selection_batch(kind):
+    """Ragged multi-request batches for the selected-output oracle.
+
+    "square": every request has exactly Hv nodes (3 requests, Hk = 2, Hv = 4,
+    d_k = 3, d_v = 5), so any (h, i) mix-up stays inside the arrays.
+    "ragged": sizes 3, 0, 7, 1, 0, 5 (empty requests and forests), Hk = 2, Hv = 4,
+    d_k = 3, d_v = 5.  "wide": 16 key / 32 value heads, d_k = 8, d_v = 6, sizes 5, 0, 9.
+    """
+    rng = np.random.default_rng({"square": 41, "ragged": 42, "wide": 43}[kind])
+    if kind == "square":
+        sizes, Hk, Hv, dk, dv = [4, 4, 4], 2, 4, 3, 5
+    elif kind == "ragged":
+        sizes, Hk, Hv, dk, dv = [3, 0, 7, 1, 0, 5], 2, 4, 3, 5
+    else:
+        sizes, Hk, Hv, dk, dv = [5, 0, 9], 16, 32, 8, 6
+    parents = []
+    for n in sizes:
+        # forests: every node after the first is a root with probability 1/4
+        par = np.array([-1 if i == 0 or rng.random() < 0.25 else int(rng.integers(0, i))
+                        for i in range(n)], np.int32)
+        parents.append(par)
+    tb = W.make_batch("sel_" + kind, 7, parents, Hk, Hv, dk, dv, "f32", W.path_random_leaf)
+    return tb
+
+
+@pytest.mark.parametrize("kind", ["square", "ragged", "wide"])
+def test_verify_selected_matches_verify(kind):
+    """oracle.verify_selected(tb, sel)[r] equals oracle.verify(tb)[offsets[b] + i, h]
+    bit for bit for every selected (b, h, i): exhaustively, and for a random
+    selection with repeats in random order."""
+    tb = _selection_batch(kind)
+    full = oracle.verify(tb)
+    offs = tb.node_offsets
+    sel = [(b, h, i) for b in range(tb.batch) for h in range(tb.n_v_heads)
+           for i in range(int(offs[b + 1] - offs[b]))]
+    rng = np.random.default_rng(5)
+    rand = [sel[j] for j in rng.integers(0, len(sel), 3 * len(sel))]
+    for chosen in (sel, rand):
+        got = oracle.verify_selected(tb, chosen, nthreads=3)
+        want = np.stack([full[offs[b] + i, h] for b, h, i in chosen])
+        np.testing.assert_array_equal(got, want)
