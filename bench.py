@@ -8,9 +8,13 @@ Default workload: batch 64, every tree 128 nodes (random, depth <= 16),
 16 key / 32 value heads, d_k = d_v = 128, bf16 q/k/v, fp32 g/beta/state.
 Inputs are seeded synthetic data resident in HBM; L2 is flushed (256 MiB
 write) between timed steps; each step is timed with CUDA events on the
-launching stream.  Prints one JSON line (rank 0).
+launching stream.  Each of the step's three calls is captured once as a CUDA
+graph through the C ABI and replayed, so that the host's per-call argument
+checks stay out of the device timing.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --configs      one line per named workload (tiny tree, chain,
+                                 best-first, ragged serving)
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (the path has no cross-request exchange): value = all ranks' node-tokens /
@@ -200,7 +204,7 @@ def summarize_clocks(lines, start=None, end=None):
 # the CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(tb, seconds: float, seed: int = 0, prepared=None):
+def oracle_sample(tb, seconds: float, seed: int = 0, prepared=None, threads=None):
     """Time the float64 oracle on a random sample of (request, value head, node)
     outputs sized to take about `seconds`; returns (node-tokens/s, threads, desc).
     The one-time conversion of the inputs to float64 (`prepared`) is not timed."""
@@ -208,7 +212,7 @@ def oracle_sample(tb, seconds: float, seed: int = 0, prepared=None):
     if prepared is None:
         prepared = oracle.prepare(tb)
     rng = np.random.default_rng(seed)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     sizes = tb.sizes()
 
     def draw(m):
@@ -255,6 +259,7 @@ def run_ours(args, rank, world, local_rank):
     status = gb.new_status(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    capture = graph_capturer(stream)
 
     def step(ev=None):
         gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes, mask, depth, words,
@@ -271,23 +276,41 @@ def run_ours(args, rank, world, local_rank):
                            max_path=tb.max_depth_bound, out=S_new, dev_status=status,
                            stream=stream)
 
-    def serving_step():
+    def serving_step(st):
         # the serving order of one decoding iteration: the previous tree's accepted
         # path committed (here the same synthetic tree's), then the new tree verified
         # from the committed state; one call, the verification launched as the
         # commit's programmatic dependent
         gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes, mask, depth, words,
-                               status, stream)
+                               status, st)
         gb.gdn_tree_commit_verify(d, d["S0"], tb.max_nodes, tb.max_depth_bound, d["q"], d["k"],
                                   d["v"], d["g"], d["beta"], d["node_offsets"], d["parent"], mask,
                                   depth, tb.max_nodes, max_depth=tb.max_depth_bound, S_new=S_new,
-                                  out=o, dev_status=status, stream=stream)
+                                  out=o, dev_status=status, stream=st)
 
+    # warm-up through the API, then each call of the step captured once as a
+    # CUDA graph (the same launches, through the same C entry points)
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     gb.check_status(status)
+    g_desc = capture(lambda st: gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                                       mask, depth, words, status, st))
+    g_verify = capture(lambda st: gb.gdn_tree_verify(
+        d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"], mask,
+        depth, tb.max_nodes, max_depth=tb.max_depth_bound, out=o, dev_status=status, stream=st))
+    g_commit = capture(lambda st: gb.gdn_tree_commit(
+        d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"],
+        d["path_offsets"], d["path_idx"], tb.max_nodes, max_path=tb.max_depth_bound, out=S_new,
+        dev_status=status, stream=st))
+    g_serv = capture(serving_step)
+    for _ in range(args.warmup):
+        flush.zero_()
+        g_desc.replay()
+        g_verify.replay()
+        g_commit.replay()
+    torch.cuda.synchronize()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -304,7 +327,11 @@ def run_ours(args, rank, world, local_rank):
         for e in evs:
             flush.zero_()
             e[0].record(stream)
-            step((e[2], e[3]))
+            g_desc.replay()
+            e[2].record(stream)
+            g_verify.replay()
+            e[3].record(stream)
+            g_commit.replay()
             e[1].record(stream)
         torch.cuda.synchronize()
         clk.mark("end")
@@ -321,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
     # one call), timed the same way
     for _ in range(args.warmup):
         flush.zero_()
-        serving_step()
+        g_serv.replay()
     torch.cuda.synchronize()
     sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
@@ -331,11 +358,13 @@ def run_ours(args, rank, world, local_rank):
     for e in sevs:
         flush.zero_()
         e[0].record(stream)
-        serving_step()
+        g_serv.replay()
         e[1].record(stream)
     torch.cuda.synchronize()
     gb.check_status(status)
-    serving_s = reduce_max(sum(e[0].elapsed_time(e[1]) for e in sevs) / 1e3, dev)
+    serv_ms = [e[0].elapsed_time(e[1]) for e in sevs]
+    serving_s = reduce_max(sum(serv_ms) / 1e3, dev)
+    del g_desc, g_verify, g_commit, g_serv
 
     # End to end through the public API, as a serving loop: the recurrent state
     # stays resident; every step uploads its inputs (the tree's q, k, v, g, beta,
@@ -432,21 +461,19 @@ def run_ours(args, rank, world, local_rank):
     cpu_v, cpu_threads, cpu_desc, _ = oracle_sample(tb, args.cpu_seconds)
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": statistics.median(step_ms), "ms_per_step_max": max(step_ms),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
-                   "tree": "random parent over nodes of depth < 16 (depth <= 16)",
-                   "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
-                   "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
-                   "step": "build_desc + verify + commit",
-                   "l2": "flushed between timed steps (256 MiB write)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(tb, args, world),
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                      "algorithmic_bytes_per_launch": vbytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "verify_only": {"us_per_launch": v_s * 1e6, "node_tokens_per_s": T / v_s,
+        "verify_only": {"us_per_launch": v_s * 1e6,
+                        "us_median": statistics.median(verify_ms) * 1e3,
+                        "us_max": max(verify_ms) * 1e3, "node_tokens_per_s": T / v_s,
                         "tflops": verify_flops(tb) / v_s / 1e12},
         "step_bytes": {"desc": desc_bytes(tb), "verify": vbytes, "commit": commit_bytes(tb)},
         "serving_order": {
@@ -454,6 +481,7 @@ def run_ours(args, rank, world, local_rank):
                      "tree verified from the committed state, the verify launched as the commit's "
                      "programmatic dependent"),
             "ms_per_step": serving_s * 1e3 / args.steps,
+            "ms_per_step_median": statistics.median(serv_ms),
             "node_tokens_per_s": job_throughput(T, args.steps, serving_s, world),
             "gpu_launches_per_step": 3},
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
@@ -469,6 +497,33 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
+
+
+def workload_config(tb, args, world) -> dict:
+    """The workload both arms report (the same keys for the GPU arm and the
+    oracle's reference arm)."""
+    return {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
+            "tree": "random parent over nodes of depth < 16 (depth <= 16)",
+            "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
+            "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
+            "step": "build_desc + verify + commit",
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
+def graph_capturer(stream):
+    """capture(fn): run fn(stream) once eagerly (first-launch set-up such as
+    shared-memory limits), then capture fn into a CUDA graph and return it."""
+    import torch
+
+    def capture(fn):
+        fn(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn(torch.cuda.current_stream())
+        return graph
+    return capture
 
 
 def dominant_kernel(tb) -> str:
@@ -504,13 +559,94 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(ts),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
-                   "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
-                   "d_v": tb.d_v, "parallelism": "host cores"},
+        "config": workload_config(tb, args, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def run_configs(args):
+    """One JSON line per named workload (tiny tree, linear chain, best-first,
+    ragged serving): step and verify throughput (node-tokens/s), the verify
+    kernel's roofline fraction, and the oracle on all host cores and on one."""
+    import torch
+    from gated_delta_net_gb300 import binding as gb
+    from gated_delta_net_gb300 import build as gbuild
+
+    gbuild.build()
+    gb.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    capture = graph_capturer(stream)
+    hbm_gbs, bf16_tf, peak_kind = load_peaks()
+    import oracle
+    workloads = [("tiny_tree", lambda: W.tiny_tree(0)), ("linear_chain", lambda: W.linear_chain(1)),
+                 ("best_first", lambda: W.best_first(2)), ("ragged_serving", lambda: W.ragged_serving(3))]
+    for name, make in workloads:
+        tb = make()
+        d = gb.upload(tb, device=dev)
+        T = tb.total_nodes
+        words = max(1, (tb.max_nodes + 31) // 32)
+        status = gb.new_status(dev)
+        mask = torch.empty((T, words), dtype=torch.int32, device=dev)
+        depth = torch.empty(T, dtype=torch.int32, device=dev)
+        o = torch.empty((T, tb.n_v_heads, tb.d_v), dtype=d["q"].dtype, device=dev)
+        S_new = torch.empty_like(d["S0"])
+        g_desc = capture(lambda st: gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                                           mask, depth, words, status, st))
+        g_verify = capture(lambda st: gb.gdn_tree_verify(
+            d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"],
+            mask, depth, tb.max_nodes, max_depth=tb.max_depth_bound, scale=tb.scale, out=o,
+            dev_status=status, stream=st))
+        g_commit = capture(lambda st: gb.gdn_tree_commit(
+            d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"],
+            d["path_offsets"], d["path_idx"], tb.max_nodes, max_path=tb.max_depth_bound,
+            out=S_new, dev_status=status, stream=st))
+        step_ms, verify_ms = [], []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            g_desc.replay()
+            e[1].record(stream)
+            g_verify.replay()
+            e[2].record(stream)
+            g_commit.replay()
+            e[3].record(stream)
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                step_ms.append(e[0].elapsed_time(e[3]))
+                verify_ms.append(e[1].elapsed_time(e[2]))
+        gb.check_status(status)
+        step_s = statistics.mean(step_ms) / 1e3
+        v_s = statistics.mean(verify_ms) / 1e3
+        vb, vf = verify_bytes(tb), verify_flops(tb)
+        t_bytes, t_flops = vb / (hbm_gbs * 1e9), vf / (bf16_tf * 1e12)
+        bound = "hbm" if t_bytes >= t_flops else "tensor"
+        prepared = oracle.prepare(tb)
+        cpu_all, threads, desc_all, _ = oracle_sample(tb, args.cpu_seconds / 2, prepared=prepared)
+        cpu_one, _, _, _ = oracle_sample(tb, args.cpu_seconds / 2, seed=1, prepared=prepared, threads=1)
+        print(json.dumps({
+            "kind": "config", "workload": tb.name, "batch": tb.batch, "n_k_heads": tb.n_k_heads,
+            "n_v_heads": tb.n_v_heads, "d": tb.d_k, "qkv": tb.qkv_dtype, "total_nodes": T,
+            "max_nodes": tb.max_nodes, "steps": args.steps, "warmup": args.warmup,
+            "step": "build_desc + verify + commit (one CUDA graph per call), L2 flushed before each step",
+            "ms_per_step": step_s * 1e3, "node_tokens_per_s": T / step_s,
+            "verify_us": v_s * 1e6, "verify_node_tokens_per_s": T / v_s,
+            "roofline": {"kernel": dominant_kernel(tb), "bound": bound,
+                         "achieved": vb / v_s / 1e9 if bound == "hbm" else vf / v_s / 1e12,
+                         "peak": hbm_gbs if bound == "hbm" else bf16_tf,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                         "frac": (t_bytes if bound == "hbm" else t_flops) / v_s,
+                         "algorithmic_bytes_per_launch": vb, "algorithmic_flops_per_launch": vf,
+                         "peak_source": peak_kind},
+            "cpu_baseline": {"kind": "oracle", "unit": UNIT, "value": cpu_all, "cores": threads,
+                             "value_one_core": cpu_one, "sample": desc_all}}), flush=True)
+        del g_desc, g_verify, g_commit, d, mask, depth, o, S_new
+        torch.cuda.empty_cache()
 
 
 def run_sweep(args):
@@ -716,6 +852,8 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--helpers", action="store_true",
                     help="time the tree relabel and row gather helpers on the throughput shapes")
+    ap.add_argument("--configs", action="store_true",
+                    help="one line per named workload: throughput, roofline, oracle on all and one core")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -727,6 +865,9 @@ def main():
         return
     if args.helpers:
         run_helpers(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
