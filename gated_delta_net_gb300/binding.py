@@ -98,6 +98,8 @@ def lib():
         L.gdn_gather_rows.restype = ctypes.c_int
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_tree_version.restype = ctypes.c_int
+        L.gdn_test_set_wait_probe.argtypes = [_I]
+        L.gdn_test_set_wait_probe.restype = None
         _lib = L
     return _lib
 
@@ -133,6 +135,12 @@ def _code(dtype: torch.dtype) -> int:
     if dtype == torch.bfloat16:
         return GDN_BF16
     raise TypeError(f"unsupported dtype {dtype}")
+
+
+def gdn_test_set_wait_probe(polls: int) -> None:
+    """Test hook: later tensor-core verify/commit launches make one bounded wait of
+    ``polls`` polls that runs out (GDN_DEV_TIMEOUT); 0 turns it off."""
+    lib().gdn_test_set_wait_probe(int(polls))
 
 
 def new_status(device=None) -> torch.Tensor:

@@ -1,4 +1,5 @@
 // api.cu -- host side of the C ABI: argument checks, kernel choice, error text.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -100,16 +101,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 int sm_count() {
-    static int count = 0;
-    if (!count) {
-        int dev = 0, c = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1)
-            return 1;
-        count = c;
-    }
-    return count;
+    // cached per device: a process may launch on devices of different sizes
+    static std::atomic<int> count[16];
+    int dev = 0, c = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 16 && (c = count[dev].load(std::memory_order_relaxed)) > 0) return c;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) return 1;
+    if (dev >= 0 && dev < 16) count[dev].store(c, std::memory_order_relaxed);
+    return c;
 }
+
+namespace {
+std::atomic<int> g_probe{0};
+}
+
+int wait_probe_polls() { return g_probe.load(std::memory_order_relaxed); }
 
 }  // namespace gdn
 
@@ -117,7 +123,9 @@ extern "C" {
 
 const char *gdn_last_error(void) { return g_err; }
 
-int gdn_tree_version(void) { return 100; }
+int gdn_tree_version(void) { return 200; }
+
+void gdn_test_set_wait_probe(int32_t polls) { gdn::g_probe.store(polls > 0 ? polls : 0); }
 
 int gdn_tree_build_desc(const int32_t *parent, const int32_t *node_offsets, int32_t batch,
                         int32_t max_nodes, uint32_t *anc_mask, int32_t mask_words,

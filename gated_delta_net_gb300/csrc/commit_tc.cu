@@ -52,10 +52,11 @@ constexpr int OFF_SCAL = OFF_COEF + kMaxPath * kMaxPath * 4;  // [2] bet, egam, 
 constexpr int kScal = 5 * kMaxPath;                           // floats per buffer
 constexpr int OFF_MISC = OFF_SCAL + 2 * kScal * 4;            // tmem slot, bad path flags [2]
 constexpr int OFF_BAR = OFF_MISC + 16;
-constexpr int kSmemBytes = OFF_BAR + 3 * 8;
+constexpr int kSmemBytes = OFF_BAR + 4 * 8;  // barriers: tile, W, U, probe (never arrived on)
 
 struct TcCommitParams {
     int hk_n, hv_n, total, items, batch, words;
+    int probe;  // > 0: thread 0 makes one wait of `probe` polls on the probe barrier (test hook)
     const float *S0;
     const int32_t *offsets, *parent, *poff, *pidx;
     const int32_t *sel_req, *sel_node;  // selected nodes (state mode)
@@ -120,15 +121,12 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
         if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
         return;
     }
-    // a verification launched as this grid's programmatic dependent may take the
-    // SMs as this grid's blocks finish (it waits for this grid before reading state)
-    griddep_launch_dependents();
     if ((int)blockIdx.x >= p.items) return;
     const int row = quad * 32 + lane, half = warp >> 2;  // tensor-memory lane = state row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     if (tid == 0) {
-        for (int k = 0; k < 3; ++k) mbar_init(&bar[k], 1);
+        for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
         fence_mbar_init();
         s_bad[0] = s_bad[1] = 0;
     }
@@ -140,7 +138,16 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // A verification launched as this grid's programmatic dependent may now take
+    // the SMs as this grid's blocks finish (it waits for this grid before reading
+    // state).  The trigger follows this block's tensor-memory allocation, so a
+    // dependent block can never hold columns that a block of this grid still
+    // waits for.
+    griddep_launch_dependents();
     bool ok = true;
+    // test hook: a bounded wait on a barrier that nothing arrives on runs out,
+    // and the block records GDN_DEV_TIMEOUT at exit; nothing else changes
+    if (p.probe > 0 && tid == 0) ok = mbar_wait(&bar[3], 0, (uint32_t)p.probe);
     uint32_t ph_tile = 0, ph_mma = 0;  // completed phases of the tile and MMA barriers
     int it = 0;                        // items committed by this block (path-data buffer = it & 1)
 
@@ -466,7 +473,7 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream) {
     p.batch = a.batch; p.S0 = a.S0;
     p.offsets = a.node_offsets; p.parent = a.parent; p.poff = a.path_offsets; p.pidx = a.path_idx;
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
-    p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
+    p.g = a.g; p.beta = a.beta; p.status = a.dev_status; p.probe = wait_probe_polls();
     static int have[16];
     cudaError_t e = ensure_smem(commit_tc_kernel<false>, kSmemBytes, have);
     if (e != cudaSuccess) return e;

@@ -69,6 +69,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // streaming multiprocessors on the current device (1 if the query fails)
 int sm_count();
 
+// Poll limit of the wait probe (0 = off), set by gdn_test_set_wait_probe.
+int wait_probe_polls();
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current device,
 // once per (kernel, device, size): `have` remembers the largest size set so far
 // per device.  Launches after the first make no attribute call, so they can be

@@ -44,7 +44,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false if the phase did not complete within `limit` polls.
+// The poll loop stays rolled: inlined at every wait, an unrolled copy would
+// multiply a kernel's code size (and its instruction-cache misses).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = (1u << 20)) {
+#pragma unroll 1
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;

@@ -190,6 +190,9 @@ typedef struct {
  * 1 <= max_depth <= 16 runs the tcgen05/TMA kernel (a deeper tree sets
  * GDN_DEV_TOO_DEEP and its request is skipped); every other case runs the
  * general kernel, which accepts any depth.
+ * q and k need no normalisation on either path (the fast path keeps the raw
+ * products k_i.k_j and q_i.k_j in fp32); non-finite inputs propagate to the
+ * outputs of the nodes below them only.
  */
 GDN_API int gdn_tree_verify(const gdn_verify_args *args, void *stream);
 
@@ -280,8 +283,8 @@ typedef struct {
  * gdn_tree_states -- the state S_i at chosen nodes i: the commit of i's own
  * root-to-node path (same section, Solution bullet 4, applied to a node that
  * is not yet accepted), so that committing one of them later needs no
- * recompute (the scope table's per-node-state variant; the pages have no
- * counterpart beyond the commit itself).  A node's path is read from its
+ * recompute (a commit applied to a node that is not yet accepted; the pages
+ * describe only the commit of the accepted path).  A node's path is read from its
  * anc_mask row (root first) and checked against parent[]; a row that does not
  * follow parent -> child edges to the node sets GDN_DEV_BAD_DESC, a selection
  * outside its request sets GDN_DEV_BAD_PATH, a path longer than 16 sets
@@ -296,6 +299,17 @@ GDN_API const char *gdn_last_error(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 GDN_API int gdn_tree_version(void);
+
+/*
+ * gdn_test_set_wait_probe -- test hook for the kernels' bounded waits (no
+ * counterpart in the pages).  With polls > 0, every later launch of the
+ * tensor-core verify and commit kernels makes one extra wait, of `polls` polls,
+ * on an mbarrier that nothing arrives on.  The wait runs out, the kernel sets
+ * GDN_DEV_TIMEOUT in *dev_status and otherwise computes and returns as usual.
+ * polls <= 0 (the default) turns the hook off.  Process-wide; not for
+ * production use.
+ */
+GDN_API void gdn_test_set_wait_probe(int32_t polls);
 
 #ifdef __cplusplus
 }

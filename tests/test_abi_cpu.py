@@ -29,13 +29,13 @@ def test_header_declares_the_entry_points():
                                          "gdn_tree_relabel",
                                          "gdn_tree_states",
                                          "gdn_tree_verify", "gdn_tree_verify_branches",
-                                         "gdn_tree_version"])
+                                         "gdn_tree_version", "gdn_test_set_wait_probe"])
 
 
 def test_library_exports_every_declared_symbol(L):
     for name in declared_symbols():
         assert hasattr(L, name), name
-    assert L.gdn_tree_version() == 100
+    assert L.gdn_tree_version() == 200
 
 
 def _verify_args(**kw):
