@@ -43,7 +43,8 @@ UNIT = "node-tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
-    "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu"],
+    "verify_tc": ["gated_delta_net_gb300/csrc/verify_tc.cu", "gated_delta_net_gb300/csrc/tc_tiles.cuh"],
+    "verify_wide": ["gated_delta_net_gb300/csrc/verify_wide.cu", "gated_delta_net_gb300/csrc/tc_tiles.cuh"],
     "verify_simt": ["gated_delta_net_gb300/csrc/verify_simt.cu"],
     "commit_tc": ["gated_delta_net_gb300/csrc/commit_tc.cu"],
 }
@@ -529,8 +530,11 @@ def graph_capturer(stream):
 def dominant_kernel(tb) -> str:
     """The verify kernel the library dispatches to (rule of include/gdn_tree.h)."""
     if (TC_READY and tb.qkv_dtype == "bf16" and tb.d_k == 128 and tb.d_v == 128
-            and tb.max_nodes <= 128 and 1 <= tb.max_depth_bound <= 16):
-        return "verify_tc"
+            and 1 <= tb.max_depth_bound <= 16):
+        if tb.max_nodes <= 128:
+            return "verify_tc"
+        if tb.max_nodes <= 256:
+            return "verify_wide"
     return "verify_simt"
 
 

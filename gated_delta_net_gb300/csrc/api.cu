@@ -79,8 +79,9 @@ cudaError_t launch_commit_any(const gdn_commit_args &a, cudaStream_t stream) {
 
 // the verification; after_commit: the preceding launch in the stream commits its state
 cudaError_t launch_verify_any(const gdn_verify_args &a, cudaStream_t stream, bool after_commit) {
-    return gdn::verify_tc_supported(a) ? gdn::launch_verify_tc(a, stream, after_commit)
-                                       : gdn::launch_verify_simt(a, stream);
+    if (gdn::verify_tc_supported(a)) return gdn::launch_verify_tc(a, stream, after_commit);
+    if (gdn::verify_wide_supported(a)) return gdn::launch_verify_wide(a, stream, after_commit);
+    return gdn::launch_verify_simt(a, stream);
 }
 
 }  // namespace

@@ -92,4 +92,8 @@ cudaError_t ensure_smem(Kernel kern, int bytes, int (&have)[16]) {
 bool verify_tc_supported(const gdn_verify_args &a);
 cudaError_t launch_verify_tc(const gdn_verify_args &a, cudaStream_t stream, bool after_commit);
 
+// the same for trees of 129 to 256 nodes (two node tiles per request)
+bool verify_wide_supported(const gdn_verify_args &a);
+cudaError_t launch_verify_wide(const gdn_verify_args &a, cudaStream_t stream, bool after_commit);
+
 }  // namespace gdn

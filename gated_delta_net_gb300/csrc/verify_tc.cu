@@ -57,15 +57,16 @@
 #include <algorithm>
 #include "internal.cuh"
 #include "sm100.cuh"
+#include "tc_tiles.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace sm100;
+using namespace tiles;
 
 constexpr int kT = 512;           // threads per block
 constexpr int kN = 128;           // tile rows: nodes (max_nodes <= 128)
-constexpr int kD = 128;           // d_k = d_v
 constexpr int kMaxDepth = 16;
 constexpr float kGammaFloor = -80.f;
 // Row stride (floats) of the raw X and Y rows: 16 entries padded to 20, so that a
@@ -161,26 +162,6 @@ __device__ bool find_unit(const TcParams &p, int idx, int end, bool report, Unit
         return true;
     }
     return false;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Byte offset of element (row, k) in a 128-row, 128-byte-swizzled bf16 tile:
-// column blocks of 64 elements (16 KB apart), rows of 128 bytes, 16-byte
-// chunks permuted by (row mod 8).  Used K-major (row = M/N index, k = K index)
-// and, for R, MN-major (row = K index j, k = N index n).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
-    return (uint32_t)((k >> 6) * 16384 + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
-}
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Node i's path within the current request: node_at[l] for l < myd (root first),
@@ -775,22 +756,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
-
-// [T][H][128] bf16 viewed as a 3-D tensor (d, head, token); boxes of 64 x 1 x 32,
-// 128-byte swizzle.
-bool encode_tokens(CUtensorMap *map, const void *base, int heads, int total) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)total};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
-    cuuint32_t box[3] = {64, 1, 32};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
 

@@ -1,0 +1,257 @@
+"""GPU parity of the tensor-core verify for trees of 129 to 256 nodes (bf16,
+d = 128, depth <= 16): two node tiles per request, block-lower-triangular P.
+
+Every case compares with the float64 oracle ("Trees from Marginals",
+gist.science Technical Summary, section 3 "Rollback-Free Tree Verification
+for GDN") at the bf16 bar, max|diff| <= 2e-2 * max|o|; batches mix requests of
+at most 128 nodes (one tile) with wider ones, since a batch whose largest tree
+has more than 128 nodes runs every request on this kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_net_gb300 import binding as gb
+from gated_delta_net_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+DEV_TOO_DEEP, DEV_BAD_DESC = 8, 32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_delta_net_gb300 import build
+    build.build()
+    gb.lib()
+
+
+def _rel(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    return float(np.max(np.abs(got - ref))) / max(float(np.max(np.abs(ref))), 1e-30)
+
+
+def _batch(seed, sizes, hk=2, hv=4, fn=None):
+    rng = np.random.default_rng(seed)
+    parents = [np.zeros(0, np.int32) if n == 0 else fn(rng, n) if fn
+               else W.depth_capped_random_tree(rng, n, 16) for n in sizes]
+    tb = W.custom(seed, parents, n_k_heads=hk, n_v_heads=hv, d=128, qkv_dtype="bf16")
+    tb.max_depth_bound = 16
+    return tb
+
+
+def _verify(tb, d=None, max_depth=16, out=None, out_dtype=None, words=None):
+    d = d or gb.upload(tb)
+    status = gb.new_status()
+    kw = {} if words is None else {"mask_words": words}
+    mask, depth = gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                         dev_status=status, **kw)
+    o = gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                           d["parent"], mask, depth, tb.max_nodes, max_depth=max_depth,
+                           scale=tb.scale, out=out, out_dtype=out_dtype, dev_status=status)
+    torch.cuda.synchronize()
+    return o, status, d
+
+
+@pytest.mark.parametrize("sizes", [(256,), (129,), (200, 1, 128, 0, 255, 130, 64),
+                                   (160, 33, 31, 32, 256)])
+def test_wide_sizes(sizes):
+    tb = _batch(sum(sizes) + 3, sizes)
+    o, status, _ = _verify(tb)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_wide_agrees_with_general_kernel():
+    tb = _batch(81, (256, 140, 7, 222))
+    o_w, st1, d = _verify(tb)
+    o_gen, st2, _ = _verify(tb, d=d, max_depth=0)
+    gb.check_status(st1)
+    gb.check_status(st2)
+    ref = oracle.verify(tb)
+    assert _rel(o_w.float().cpu().numpy(), ref) <= TOL_BF16
+    assert _rel(o_gen.float().cpu().numpy(), ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("shape", ["star", "binary", "all_roots", "chains"])
+def test_wide_tree_shapes(shape):
+    # a root with 255 children (its descendant row spans all eight words), a
+    # complete binary tree of 255 nodes (depth 8, ancestors across both tiles),
+    # 256 roots, and sixteen chains of 16 whose later chains sit in the second tile
+    if shape == "star":
+        par = np.array([-1] + [0] * 255, np.int32)
+    elif shape == "binary":
+        par = np.array([-1] + [(i - 1) // 2 for i in range(1, 255)], np.int32)
+    elif shape == "all_roots":
+        par = np.full(256, -1, np.int32)
+    else:
+        par = np.array([-1 if i % 16 == 0 else i - 1 for i in range(256)], np.int32)
+    tb = _batch(62, (len(par), len(par), 90), fn=lambda r, n: par if n == len(par) else
+                W.depth_capped_random_tree(r, n, 16))
+    o, status, _ = _verify(tb)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_wide_chain16_across_the_tile_boundary():
+    # one chain of 16 from node 120 to node 135 under a root chain: the path of a
+    # second-tile node runs through first-tile ancestors (the P21 block)
+    par = np.array([-1] + list(range(0, 119)) + [-1] + list(range(120, 135)) +
+                   [-1] * 120, np.int32)
+    par[1:120] = np.where(np.arange(1, 120) % 15 == 0, -1, par[1:120])
+    tb = _batch(63, (len(par),), hk=1, hv=2, fn=lambda r, n: par)
+    depth = np.zeros(len(par), np.int64)
+    for i, a in enumerate(par):
+        depth[i] = 1 if a < 0 else depth[a] + 1
+    assert depth.max() == 16 and depth[135] == 16
+    o, status, _ = _verify(tb)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_wide_fp32_output_and_scale():
+    tb = _batch(64, (256, 150))
+    tb.scale = 0.25
+    o, status, _ = _verify(tb, out_dtype=torch.float32)
+    gb.check_status(status)
+    assert o.dtype == torch.float32
+    assert _rel(o.cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_wide_rejects_deeper_tree():
+    tb = _batch(65, (200, 30), fn=lambda r, n: W.chain_tree(n))
+    _, status, _ = _verify(tb)
+    assert int(status.item()) & DEV_TOO_DEEP
+
+
+def test_wide_non_finite_inputs_stay_on_their_branch():
+    rng = np.random.default_rng(13)
+    parent = W.depth_capped_random_tree(rng, 256, max_depth=12)
+    base_tb = _batch(13, (256,), hk=1, hv=2, fn=lambda r, n: parent)
+    base, st, _ = _verify(base_tb)
+    gb.check_status(st)
+    for bad_node in (0, 5, 127, 128, 201):
+        sub = {bad_node}
+        for i in range(256):
+            if parent[i] in sub:
+                sub.add(i)
+        keep = [i for i in range(256) if i not in sub]
+        for val in (np.nan, np.inf):
+            tb2 = _batch(13, (256,), hk=1, hv=2, fn=lambda r, n: parent)
+            tb2.k[bad_node] = val
+            tb2.v[bad_node] = val
+            tb2.g[bad_node] = val
+            o2, st2, _ = _verify(tb2)
+            gb.check_status(st2)
+            assert torch.equal(o2[keep], base[keep])
+
+
+def _mixed_sizes(count):
+    cycle = (0, 1, 33, 256, 7, 129, 200, 2, 128)
+    return tuple(cycle[i % len(cycle)] for i in range(count))
+
+
+def test_wide_many_items_per_block():
+    # 180 requests x 4 value heads: more items than resident blocks, so each
+    # persistent block runs several items of mixed sizes (and skips empty ones)
+    tb = _batch(23, _mixed_sizes(180))
+    o, status, _ = _verify(tb)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_wide_bad_request_among_many_is_skipped():
+    tb = _batch(24, _mixed_sizes(180))
+    d = gb.upload(tb)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                         dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    bad = 15                                   # a request of 200 nodes
+    lo, hi = int(tb.node_offsets[bad]), int(tb.node_offsets[bad + 1])
+    assert hi - lo == 200
+    depth[lo + 170] += 1                       # stale descriptor row in the second tile
+    out = torch.full((tb.total_nodes, tb.n_v_heads, tb.d_v), 5.0, dtype=torch.bfloat16,
+                     device=d["q"].device)
+    gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                       d["parent"], mask, depth, tb.max_nodes, max_depth=16, out=out,
+                       dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == DEV_BAD_DESC
+    assert torch.all(out[lo:hi] == 5.0)        # the malformed request is skipped
+    ref = oracle.verify(tb)
+    keep = np.r_[0:lo, hi:tb.total_nodes]
+    assert _rel(out.float().cpu().numpy()[keep], ref[keep]) <= TOL_BF16
+
+
+def test_wide_stray_bit_past_the_tree_is_a_stale_descriptor():
+    # descriptor rows of eight words for trees of at most 180 nodes: the words
+    # past the tree are read and must be empty
+    tb = _batch(25, (180, 97, 150))
+    o6, status6, d = _verify(tb)
+    gb.check_status(status6)
+    o, status, _ = _verify(tb, d=d, words=8)
+    gb.check_status(status)
+    assert torch.equal(o, o6)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(d["parent"], d["node_offsets"], tb.max_nodes,
+                                         mask_words=8, dev_status=status)
+    torch.cuda.synchronize()
+    mask[5, 7] = 1                             # request 0, node 5: a bit for node 224
+    out = torch.full((tb.total_nodes, tb.n_v_heads, tb.d_v), 3.0, dtype=torch.bfloat16,
+                     device=d["q"].device)
+    gb.gdn_tree_verify(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"],
+                       d["parent"], mask, depth, tb.max_nodes, max_depth=16, out=out,
+                       dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == DEV_BAD_DESC
+    assert torch.all(out[:180] == 3.0)         # the request is skipped
+    assert torch.equal(out[180:], o6[180:])
+
+
+def test_wide_leaves_S0_untouched():
+    tb = _batch(26, (256, 256))
+    d = gb.upload(tb)
+    before = d["S0"].clone()
+    _verify(tb, d=d)
+    assert torch.equal(before, d["S0"])
+
+
+def test_wide_wait_probe_times_out_and_returns():
+    tb = _batch(27, (256, 133, 256))
+    o0, st, d = _verify(tb)
+    gb.check_status(st)
+    try:
+        gb.gdn_test_set_wait_probe(2000)
+        o1, st1, _ = _verify(tb, d=d)
+        bits = int(st1.item())
+    finally:
+        gb.gdn_test_set_wait_probe(0)
+    assert bits == 16
+    assert torch.equal(o1, o0)
+    o2, st2, _ = _verify(tb, d=d)
+    gb.check_status(st2)
+    assert torch.equal(o2, o0)
+
+
+def test_wide_commit_verify_serving_order():
+    # the committed state of the previous tree feeds the verify of the next one,
+    # the verify launched as the commit's programmatic dependent
+    prev = _batch(28, (256, 180))
+    new = _batch(29, (256, 200))
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes,
+                                         dev_status=status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 16, dn["q"], dn["k"], dn["v"],
+                                     dn["g"], dn["beta"], dn["node_offsets"], dn["parent"], mask,
+                                     depth, new.max_nodes, max_depth=16, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S_ref, st = oracle.commit(prev)
+    assert st == 0
+    new.S0 = S_ref.astype(np.float32)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
