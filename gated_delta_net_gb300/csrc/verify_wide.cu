@@ -14,18 +14,20 @@
 // topologically, a node of T1 has its ancestors in T1, so P is block-lower-
 // triangular: O_T1 = e^gamma Z_T1 + P11 R_T1 and O_T2 = e^gamma Z_T2 + P21 R_T1 + P22 R_T2.
 //
-// One block of 256 threads per SM walks (request, value head) items; thread t is
-// node t.  Per item, in order:
+// One block of 256 threads per SM walks a contiguous range of (request, value
+// head) items; thread t is node t.  Per item, in order:
 //   1. K and Q of all nodes by TMA; node data (paths, gamma, descriptor checks,
-//      descendant rows); S0 to bf16.
+//      descendant rows; kept while the request stays); S0 to bf16.
 //   2. Gram of the ancestors in T1: K_T1 [K;Q]^T (N = 256 + 256, all 512 tensor-
 //      memory columns), scattered into raw X and Y rows of every descendant; then
 //      the Gram of the ancestors in T2: K_T2 [K_T2;Q_T2]^T, scattered likewise.
+//      The raw rows hold no value-head data, so the next value head of the same
+//      key head keeps them and skips this step (its K and Q come again from L2).
 //   3. W = K S0^T and Z = Q S0^T for both tiles (512 columns); V of both tiles by
 //      TMA into the K space; P rows into the Q and S0 spaces (P11 | P21 | P22).
 //   4. R over V; Z_T1 += P11 R_T1, Z_T2 += P21 R_T1 + P22 R_T2; the epilogue,
 //      staged over R and stored by TMA.
-// Every mbarrier completes once per item; every wait is bounded, and a timeout
+// Every mbarrier completes once per item (the Gram's once per Gram); every wait is bounded, and a timeout
 // sets GDN_DEV_TIMEOUT.  A non-finite right-hand side row is replaced by zero in
 // the output products and its subtree's outputs are set to NaN.
 #include <algorithm>
@@ -77,10 +79,10 @@ struct Item {
     int idx, b, hv, hk, lo, n;
 };
 
-// The first item at or after idx (a stride of the grid) whose request is
-// non-empty and well placed; others are flagged (when `report`) and passed over.
-__device__ bool find_item(const WideParams &p, int idx, bool report, Item &it) {
-    for (; idx < p.items; idx += gridDim.x) {
+// The first item in [idx, end) whose request is non-empty and well placed;
+// others are flagged (when `report`) and passed over.
+__device__ bool find_item(const WideParams &p, int idx, int end, bool report, Item &it) {
+    for (; idx < end; ++idx) {
         const int b = idx / p.hv_n;
         const int lo = __ldg(p.offsets + b);
         const int n = __ldg(p.offsets + b + 1) - lo;
@@ -125,8 +127,11 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (tid == 0) flag(p.status, GDN_DEV_INTERNAL);
         return;
     }
+    // a contiguous range of items per block, so that the value heads of one key
+    // head follow each other and share the tree data, the Gram and its scatter
+    const int end = (int)(((int64_t)(blockIdx.x + 1) * p.items) / gridDim.x);
     Item cur;
-    if (!find_item(p, blockIdx.x, tid == 0, cur)) {
+    if (!find_item(p, (int)(((int64_t)blockIdx.x * p.items) / gridDim.x), end, tid == 0, cur)) {
         griddep_wait();  // the block ends after the preceding grid, like the others
         return;
     }
@@ -151,10 +156,17 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
     const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
 
+    int prev_b = -1, prev_hk = -1, gph = 0;
     for (int it = 0;; ++it) {
         const int ph = it & 1;
         const int n = cur.n, nb = (n + 31) >> 5;
         const bool two = n > 128;  // block-uniform: the second tile has nodes
+        const bool same_req = cur.b == prev_b;               // tree data kept
+        const bool same_kh = same_req && cur.hk == prev_hk;  // raw X and Y rows kept too
+        prev_b = cur.b;
+        prev_hk = cur.hk;
+        Item nx;
+        const bool more = find_item(p, cur.idx + 1, end, tid == 0, nx);
         // ---- 1. K and Q tiles; node data; S0 as bf16 --------------------------
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar[W_KQ], (uint32_t)(2 * 2 * nb * 4096));
@@ -171,26 +183,32 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         float gr = 0.f, br = 0.f;
         if (i < n) {
             const int64_t gi = cur.lo + i;
-            pi = __ldg(p.parent + gi);
-            di = __ldg(p.depth + gi);
+            if (!same_req) {
+                pi = __ldg(p.parent + gi);
+                di = __ldg(p.depth + gi);
 #pragma unroll
-            for (int w = 0; w < kWords; ++w) mw[w] = w < p.words ? __ldg(p.mask + gi * p.stride + w) : 0u;
+                for (int w = 0; w < kWords; ++w) mw[w] = w < p.words ? __ldg(p.mask + gi * p.stride + w) : 0u;
+            }
             gr = __ldg(p.g + gi * p.hv_n + cur.hv);
             br = __ldg(p.beta + gi * p.hv_n + cur.hv);
         }
-        par[i] = pi;
-        dep[i] = di;
+        if (!same_req) {
+            par[i] = pi;
+            dep[i] = di;
 #pragma unroll
-        for (int w = 0; w < kWords; ++w) msk[i * kWords + w] = mw[w];
+            for (int w = 0; w < kWords; ++w) msk[i * kWords + w] = mw[w];
+            if (i == 0) *s_err = 0;
+        }
+        if (!same_kh) {
+#pragma unroll
+            for (int q = 0; q < kXS / 4; ++q) {
+                reinterpret_cast<float4 *>(Xs + i * kXS)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(Ys + i * kXS)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         graw[i] = gr;
         bet[i] = br;
-#pragma unroll
-        for (int q = 0; q < kXS / 4; ++q) {
-            reinterpret_cast<float4 *>(Xs + i * kXS)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            reinterpret_cast<float4 *>(Ys + i * kXS)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
         if (i < 8) pset[i] = 0u;
-        if (i == 0) *s_err = 0;
         // S0 rows 16 warp .. 16 warp + 15 as bf16 (B operand, K-major, 128-byte
         // swizzle); lane l holds columns 4l .. 4l + 3 (coalesced row reads)
         {
@@ -211,7 +229,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         __syncthreads();
         // validation: parent in [-1, i), depth and mask row consistent with the parent's
-        if (i < n) {
+        if (i < n && !same_req) {
             int e = 0;
             if (pi < -1 || pi >= i) {
                 e = GDN_DEV_BAD_TREE;
@@ -241,7 +259,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
         }
         // node i's path (i itself past the depth, so every index stays in range)
-        const int myd = i < n ? min(max(di, 0), kMaxDepth) : 0;
+        const int myd = i < n ? min(max(dep[i], 0), kMaxDepth) : 0;
         int node_at[kMaxDepth];
         {
             const uint4 pr = *reinterpret_cast<const uint4 *>(path + i * kMaxDepth);
@@ -266,7 +284,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
         for (int c = 0; c < kWords; ++c) {
             mine[c] = 0u;
-            if (c > warp) continue;  // warp-uniform
+            if (c > warp || same_req) continue;  // warp-uniform
             uint32_t x = __brev(mw[c]);
             uint32_t m = 0x0000FFFFu;
 #pragma unroll
@@ -277,12 +295,14 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             mine[c] = __brev(x);
         }
         __syncthreads();  // every ancestor row has been read by the validation
+        if (!same_req) {
 #pragma unroll
-        for (int c = 0; c < kWords; ++c) msk[(c * 32 + lane) * kWords + warp] = mine[c];
+            for (int c = 0; c < kWords; ++c) msk[(c * 32 + lane) * kWords + warp] = mine[c];
+        }
         fence_proxy_async_smem();  // S0 bf16 is read by the tensor cores
         __syncthreads();
         const bool item_good = *s_err == 0;
-        if (i == 0 && !item_good) flag(p.status, *s_err);
+        if (i == 0 && !item_good && !same_req) flag(p.status, *s_err);
 
         // ---- 2. the Gram of the ancestors in T1, then in T2, scattered -------
         // lane a holds k_a.k_j and k_a.q_j and writes them into the raw ancestor
@@ -312,6 +332,9 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (tid == 0) {
             ok = mbar_wait(&bar[W_KQ], ph) && ok;
             tc_fence_after();
+        }
+        if (!same_kh) {  // block-uniform
+        if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kadr = smem_u32(sm + OFF_K + (ks >> 2) * 32768 + (ks & 3) * 32);
@@ -322,7 +345,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
             mma_commit(&bar[W_G1]);
         }
-        ok = mbar_wait(&bar[W_G1], ph) && ok;
+        ok = mbar_wait(&bar[W_G1], gph) && ok;
         tc_fence_after();
         // ancestors in T1: lanes quad * 32 + lane, chunks quad .. 7 of all 256 columns
         scatter(quad * 32 + lane, quad, 0, tmem, tmem + 256);
@@ -330,7 +353,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         mbar_arrive(&bar[W_SC1]);
         if (tid == 0) {
             if (two) {
-                ok = mbar_wait(&bar[W_SC1], ph) && ok;  // the first Gram has been read out
+                ok = mbar_wait(&bar[W_SC1], gph) && ok;  // the first Gram has been read out
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -345,8 +368,8 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 mbar_arrive(&bar[W_G2]);
             }
         }
-        ok = mbar_wait(&bar[W_G2], ph) && ok;
-        ok = mbar_wait(&bar[W_SC1], ph) && ok;  // every T1 ancestor's entries are in
+        ok = mbar_wait(&bar[W_G2], gph) && ok;
+        ok = mbar_wait(&bar[W_SC1], gph) && ok;  // every T1 ancestor's entries are in
         if (two) {
             tc_fence_after();
             // ancestors in T2: lanes 128 + quad * 32 + lane, chunks 4 + quad .. 7
@@ -354,10 +377,12 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         tc_fence_before();
         mbar_arrive(&bar[W_SC2]);
+        ok = mbar_wait(&bar[W_SC2], gph) && ok;  // every X and Y entry is in, the Gram columns are free
+        gph ^= 1;
+        }  // !same_kh
 
         // ---- 3. S0 part, V, P rows --------------------------------------------
         if (tid == 0) {
-            ok = mbar_wait(&bar[W_SC2], ph) && ok;  // the Gram columns are free
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -384,7 +409,6 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                                 cur.lo + 128 + 32 * r);
             }
         }
-        ok = mbar_wait(&bar[W_SC2], ph) && ok;  // every X and Y entry is in
         float P[kMaxDepth];
         {
 #pragma unroll
@@ -553,8 +577,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             bulk_wait_read();  // the K space may be loaded again
         }
         __syncthreads();
-        Item nx;
-        if (!find_item(p, cur.idx + gridDim.x, tid == 0, nx)) break;
+        if (!more) break;
         cur = nx;
     }
     if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
