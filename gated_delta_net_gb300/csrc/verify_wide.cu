@@ -16,20 +16,23 @@
 //
 // One block of 256 threads per SM walks a contiguous range of (request, value
 // head) items; thread t is node t.  Per item, in order:
-//   1. K and Q of all nodes by TMA; node data (paths, gamma, descriptor checks,
-//      descendant rows; kept while the request stays); S0 to bf16.
+//   1. node data (paths, gamma, descriptor checks, descendant rows; kept while
+//      the request stays); K and Q arrive by TMA, S0 is already bf16.
 //   2. Gram of the ancestors in T1: K_T1 [K;Q]^T (N = 256 + 256, all 512 tensor-
 //      memory columns), scattered into raw X and Y rows of every descendant; then
-//      the Gram of the ancestors in T2: K_T2 [K_T2;Q_T2]^T, scattered likewise.
-//      The raw rows hold no value-head data, so the next value head of the same
-//      key head keeps them and skips this step (its K and Q come again from L2).
-//   3. W = K S0^T and Z = Q S0^T for both tiles (512 columns); V of both tiles by
-//      TMA into the K space; P rows into the Q and S0 spaces (P11 | P21 | P22).
-//   4. R over V; Z_T1 += P11 R_T1, Z_T2 += P21 R_T1 + P22 R_T2; the epilogue,
-//      staged over R and stored by TMA.
-// Every mbarrier completes once per item (the Gram's once per Gram); every wait is bounded, and a timeout
-// sets GDN_DEV_TIMEOUT.  A non-finite right-hand side row is replaced by zero in
-// the output products and its subtree's outputs are set to NaN.
+//      Z = Q S0^T and the Gram of the ancestors in T2, K_T2 [K_T2;Q_T2]^T, which
+//      frees the Q space for V; the second scatter; W = K S0^T.  The raw rows hold
+//      no value-head data, so the next value head of the same key head keeps them
+//      and skips the Grams (its K and Q come again, from L2).
+//   3. P rows into the K and S0 spaces (P11 | P21 | P22); R over V; Z_T1 += P11
+//      R_T1, Z_T2 += P21 R_T1 + P22 R_T2.
+//   4. The next item's fp32 state tile by bulk copy into the K space (free once
+//      the output products are done) while the epilogue runs, staged over R and
+//      stored by TMA; then the state tile to bf16, and the next K and Q loads.
+// Every mbarrier completes once per item (the Gram's once per Gram); every wait
+// is bounded, and a timeout sets GDN_DEV_TIMEOUT.  A non-finite right-hand side
+// row is replaced by zero in the output products and its subtree's outputs are
+// set to NaN.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -50,18 +53,21 @@ constexpr int kXS = 20;           // row stride (floats) of the raw X and Y rows
 constexpr int kWords = 8;         // mask words per node
 
 // shared-memory layout (bytes from the dynamic base, which is 1024-aligned)
-constexpr int OFF_K = 0;          // K [2 k-blocks][256 rows][128 B]; then V|R|outputs of T1 (+0) and T2 (+32 KB)
-constexpr int OFF_Q = 65536;      // Q [2 k-blocks][256 rows][128 B]; then P11 (+0) and P21 (+32 KB)
+constexpr int OFF_K = 0;          // K [2 k-blocks][256 rows][128 B]; then P11 (+0) and P21 (+32 KB); then the next S0 (fp32)
+constexpr int OFF_Q = 65536;      // Q [2 k-blocks][256 rows][128 B]; then V|R|outputs of T1 (+0) and T2 (+32 KB)
 constexpr int OFF_S0 = 131072;    // S0 bf16 [2 k-blocks][128][128 B]; then P22
 constexpr int OFF_X = 163840;     // float [256][kXS] raw k.k of strict ancestors
 constexpr int OFF_Y = OFF_X + kNW * kXS * 4;            // float [256][kXS] raw q.k of ancestors
 constexpr int OFF_MASK = OFF_Y + kNW * kXS * 4;         // uint32 [256][8] ancestor, then descendant rows
 constexpr int OFF_PATH = OFF_MASK + kNW * kWords * 4;   // uint8 [256][16]
-constexpr int OFF_F = OFF_PATH + kNW * kMaxDepth;       // float graw, gam, egt, eg, bet [256]
-constexpr int OFF_I = OFF_F + 5 * kNW * 4;              // int dep, par [256]
+constexpr int OFF_F = OFF_PATH + kNW * kMaxDepth;       // float [2 items][graw, gam, egt, eg, bet][256]
+constexpr int OFF_I = OFF_F + 2 * 5 * kNW * 4;          // int dep, par [256]
 constexpr int OFF_MISC = OFF_I + 2 * kNW * 4;           // tmem slot; pset[8]; err
 constexpr int OFF_BAR = OFF_MISC + 64;
-enum { W_KQ, W_G1, W_SC1, W_G2, W_SC2, W_S0, W_V, W_OUT, W_PROBE, W_BARS };
+// K, Q arrived; first Gram done, scattered; Q products done (the Q space is
+// free); second scatter; W done (the K and S0 spaces are free); V arrived;
+// output products done; next state tile arrived; wait probe
+enum { W_K, W_Q, W_G1, W_SC1, W_G2, W_SC2, W_S0M, W_V, W_OUT, W_S0F, W_PROBE, W_BARS };
 constexpr int kSmemBytes = OFF_BAR + W_BARS * 8;
 
 struct WideParams {
@@ -102,6 +108,21 @@ __device__ bool find_item(const WideParams &p, int idx, int end, bool report, It
     return false;
 }
 
+// Thread 0: the item's fp32 state tile (64 KB, contiguous) into the K space.
+__device__ __forceinline__ void issue_state(const WideParams &p, const Item &it, uint8_t *sm, uint64_t *bar) {
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD));
+    mbar_arrive_expect_tx(bar, 65536u);
+    for (int c = 0; c < 4; ++c) bulk_load(sm + OFF_K + c * 16384, src + c * 16384, 16384u, bar);
+}
+
+// Thread 0: the item's K or Q rows (boxes of 32 nodes, both 64-column halves).
+__device__ __forceinline__ void issue_tokens(const CUtensorMap *map, const Item &it, uint8_t *dst, uint64_t *bar) {
+    const int nb = (it.n + 31) >> 5;
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * nb * 4096));
+    for (int kb = 0; kb < 2; ++kb)
+        for (int r = 0; r < nb; ++r) tma_load_3d(dst + kb * 32768 + r * 4096, map, bar, kb * 64, it.hk, it.lo + 32 * r);
+}
+
 template <typename Tout>
 __global__ void __launch_bounds__(kT, 1)
 verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
@@ -111,8 +132,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     float *Ys = reinterpret_cast<float *>(sm + OFF_Y);
     uint32_t *msk = reinterpret_cast<uint32_t *>(sm + OFF_MASK);
     uint8_t *path = sm + OFF_PATH;
-    float *graw = reinterpret_cast<float *>(sm + OFF_F);
-    float *gam = graw + kNW, *egt = graw + 2 * kNW, *eg = graw + 3 * kNW, *bet = graw + 4 * kNW;
+    float *fbase = reinterpret_cast<float *>(sm + OFF_F);
     int *dep = reinterpret_cast<int *>(sm + OFF_I), *par = dep + kNW;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     uint32_t *pset = tslot + 1;                       // [8]: nodes whose output is poisoned
@@ -155,6 +175,38 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     griddep_wait();  // S0 may be the output of a preceding grid
 
     const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
+    const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
+
+    // The fp32 state tile in the K space to bf16 in the S0 space (B operand,
+    // K-major, 128-byte swizzle): rows 16 warp .. 16 warp + 15, lane l holds
+    // columns 4l .. 4l + 3; then the K space takes the item's keys.
+    int sph = 0;
+    auto convert_state = [&](const Item &it) {
+        ok = mbar_wait(&bar[W_S0F], sph) && ok;
+        sph ^= 1;
+        float4 sa[8], sb[8];
+        const float4 *src = reinterpret_cast<const float4 *>(sm + OFF_K);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            sa[r] = src[(warp * 16 + r) * 32 + lane];
+            sb[r] = src[(warp * 16 + 8 + r) * 32 + lane];
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + r, 4 * lane)) =
+                make_uint2(pack_bf16(sa[r].x, sa[r].y), pack_bf16(sa[r].z, sa[r].w));
+            *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + 8 + r, 4 * lane)) =
+                make_uint2(pack_bf16(sb[r].x, sb[r].y), pack_bf16(sb[r].z, sb[r].w));
+        }
+        fence_proxy_async_smem();  // the bf16 tile is read, the K space written, by the async proxy
+        __syncthreads();
+        if (tid == 0) issue_tokens(&tmK, it, sm + OFF_K, &bar[W_K]);
+    };
+    if (tid == 0) {
+        issue_state(p, cur, sm, &bar[W_S0F]);
+        issue_tokens(&tmQ, cur, sm + OFF_Q, &bar[W_Q]);
+    }
+    convert_state(cur);
 
     int prev_b = -1, prev_hk = -1, gph = 0;
     for (int it = 0;; ++it) {
@@ -167,28 +219,29 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         prev_hk = cur.hk;
         Item nx;
         const bool more = find_item(p, cur.idx + 1, end, tid == 0, nx);
-        // ---- 1. K and Q tiles; node data; S0 as bf16 --------------------------
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar[W_KQ], (uint32_t)(2 * 2 * nb * 4096));
-            for (int kb = 0; kb < 2; ++kb)
-                for (int r = 0; r < nb; ++r) {
-                    tma_load_3d(sm + OFF_K + kb * 32768 + r * 4096, &tmK, &bar[W_KQ], kb * 64, cur.hk, cur.lo + 32 * r);
-                    tma_load_3d(sm + OFF_Q + kb * 32768 + r * 4096, &tmQ, &bar[W_KQ], kb * 64, cur.hk, cur.lo + 32 * r);
-                }
+        // per-head node data (g, beta, decay sums) of this item, and of the next one
+        // when it is another value head of the same request (made during this item)
+        float *graw = fbase + ph * 5 * kNW;
+        float *gam = graw + kNW, *egt = graw + 2 * kNW, *eg = graw + 3 * kNW, *bet = graw + 4 * kNW;
+        float *graw_n = fbase + (ph ^ 1) * 5 * kNW;
+        const bool pre_next = more && nx.b == cur.b;
+        float gr_n = 0.f, br_n = 0.f;  // in flight during the item
+        if (pre_next && i < n) {
+            gr_n = __ldg(p.g + (int64_t)(nx.lo + i) * p.hv_n + nx.hv);
+            br_n = __ldg(p.beta + (int64_t)(nx.lo + i) * p.hv_n + nx.hv);
         }
+        // ---- 1. node data -------------------------------------------------------
         int pi = -1, di = 0;
         uint32_t mw[kWords];
 #pragma unroll
         for (int w = 0; w < kWords; ++w) mw[w] = 0u;
         float gr = 0.f, br = 0.f;
-        if (i < n) {
+        if (i < n && !same_req) {
             const int64_t gi = cur.lo + i;
-            if (!same_req) {
-                pi = __ldg(p.parent + gi);
-                di = __ldg(p.depth + gi);
+            pi = __ldg(p.parent + gi);
+            di = __ldg(p.depth + gi);
 #pragma unroll
-                for (int w = 0; w < kWords; ++w) mw[w] = w < p.words ? __ldg(p.mask + gi * p.stride + w) : 0u;
-            }
+            for (int w = 0; w < kWords; ++w) mw[w] = w < p.words ? __ldg(p.mask + gi * p.stride + w) : 0u;
             gr = __ldg(p.g + gi * p.hv_n + cur.hv);
             br = __ldg(p.beta + gi * p.hv_n + cur.hv);
         }
@@ -206,27 +259,11 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 reinterpret_cast<float4 *>(Ys + i * kXS)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        graw[i] = gr;
-        bet[i] = br;
-        if (i < 8) pset[i] = 0u;
-        // S0 rows 16 warp .. 16 warp + 15 as bf16 (B operand, K-major, 128-byte
-        // swizzle); lane l holds columns 4l .. 4l + 3 (coalesced row reads)
-        {
-            const float *s0t = p.S0 + ((int64_t)cur.b * p.hv_n + cur.hv) * (kD * kD);
-            float4 sa[8], sb[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                sa[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (warp * 16 + r) * kD) + lane);
-                sb[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (warp * 16 + 8 + r) * kD) + lane);
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + r, 4 * lane)) =
-                    make_uint2(pack_bf16(sa[r].x, sa[r].y), pack_bf16(sa[r].z, sa[r].w));
-                *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + 8 + r, 4 * lane)) =
-                    make_uint2(pack_bf16(sb[r].x, sb[r].y), pack_bf16(sb[r].z, sb[r].w));
-            }
+        if (!same_req) {
+            graw[i] = gr;
+            bet[i] = br;
         }
+        if (i < 8) pset[i] = 0u;
         __syncthreads();
         // validation: parent in [-1, i), depth and mask row consistent with the parent's
         if (i < n && !same_req) {
@@ -267,14 +304,16 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
             for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0xFFu) : i;
         }
-        {
+        // decay sums along the path (made by the previous item for the same request)
+        auto decay_sums = [&](float *f) {
             float acc = 0.f;
 #pragma unroll
-            for (int l = 0; l < kMaxDepth; ++l) acc += l < myd ? graw[node_at[l]] : 0.f;
-            gam[i] = acc;
-            egt[i] = i < n ? expf(acc) : 0.f;
-            eg[i] = i < n ? expf(fmaxf(acc, kGammaFloor)) : 1.f;
-        }
+            for (int l = 0; l < kMaxDepth; ++l) acc += l < myd ? f[node_at[l]] : 0.f;
+            f[kNW + i] = acc;
+            f[2 * kNW + i] = i < n ? expf(acc) : 0.f;
+            f[3 * kNW + i] = i < n ? expf(fmaxf(acc, kGammaFloor)) : 1.f;
+        };
+        if (!same_req) decay_sums(graw);
         // mask rows become descendant rows: bit i of row a iff a is on i's path.
         // Warp w owns word w of every row: the transpose of the 32 x 32 bit block
         // (its nodes i) x (word c of their ancestor rows), by five rounds of
@@ -299,12 +338,11 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
             for (int c = 0; c < kWords; ++c) msk[(c * 32 + lane) * kWords + warp] = mine[c];
         }
-        fence_proxy_async_smem();  // S0 bf16 is read by the tensor cores
         __syncthreads();
         const bool item_good = *s_err == 0;
         if (i == 0 && !item_good && !same_req) flag(p.status, *s_err);
 
-        // ---- 2. the Gram of the ancestors in T1, then in T2, scattered -------
+        // ---- 2. Grams, scatters and the state products -----------------------------
         // lane a holds k_a.k_j and k_a.q_j and writes them into the raw ancestor
         // rows of its descendants j (X strict, Y inclusive); the warps of both
         // groups share a lane quarter and take alternate 32-column chunks
@@ -329,86 +367,109 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     if ((dm >> c) & 1u) Ys[(cc * 32 + c) * kXS + da - 1] = __uint_as_float(v[c]);
             }
         };
-        if (tid == 0) {
-            ok = mbar_wait(&bar[W_KQ], ph) && ok;
-            tc_fence_after();
-        }
-        if (!same_kh) {  // block-uniform
-        if (tid == 0) {
+        // k-step ks of a 128-row operand at `base` (two 16 KB k-blocks per 128 rows)
+        auto kdesc = [&](int off, int ks) {
+            return smem_desc(smem_u32(sm + off + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2);
+        };
+        auto sdesc = [&](int ks) {  // S0 bf16: 128 rows, k-blocks of 16 KB
+            return smem_desc(smem_u32(sm + OFF_S0 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
+        };
+        // Z_t = Q_t S0^T into columns 256 + 128 t
+        auto issue_z = [&]() {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kadr = smem_u32(sm + OFF_K + (ks >> 2) * 32768 + (ks & 3) * 32);
-                const uint32_t qadr = smem_u32(sm + OFF_Q + (ks >> 2) * 32768 + (ks & 3) * 32);
-                const uint64_t a = smem_desc(kadr, 16, 1024, 2);
-                mma_bf16(tmem, a, a, id_n256, ks > 0);                                 // K_T1 K^T (N = 256)
-                mma_bf16(tmem + 256, a, smem_desc(qadr, 16, 1024, 2), id_n256, ks > 0);  // K_T1 Q^T
+                mma_bf16(tmem + 256, kdesc(OFF_Q, ks), sdesc(ks), id_n128, ks > 0);
+                if (two) mma_bf16(tmem + 384, kdesc(OFF_Q + 16384, ks), sdesc(ks), id_n128, ks > 0);
             }
-            mma_commit(&bar[W_G1]);
-        }
-        ok = mbar_wait(&bar[W_G1], gph) && ok;
-        tc_fence_after();
-        // ancestors in T1: lanes quad * 32 + lane, chunks quad .. 7 of all 256 columns
-        scatter(quad * 32 + lane, quad, 0, tmem, tmem + 256);
-        tc_fence_before();
-        mbar_arrive(&bar[W_SC1]);
-        if (tid == 0) {
-            if (two) {
-                ok = mbar_wait(&bar[W_SC1], gph) && ok;  // the first Gram has been read out
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kadr = smem_u32(sm + OFF_K + (ks >> 2) * 32768 + 16384 + (ks & 3) * 32);
-                    const uint32_t qadr = smem_u32(sm + OFF_Q + (ks >> 2) * 32768 + 16384 + (ks & 3) * 32);
-                    const uint64_t a = smem_desc(kadr, 16, 1024, 2);
-                    mma_bf16(tmem, a, a, id_n128, ks > 0);                                 // K_T2 K_T2^T
-                    mma_bf16(tmem + 128, a, smem_desc(qadr, 16, 1024, 2), id_n128, ks > 0);  // K_T2 Q_T2^T
-                }
-                mma_commit(&bar[W_G2]);
-            } else {
-                mbar_arrive(&bar[W_G2]);
-            }
-        }
-        ok = mbar_wait(&bar[W_G2], gph) && ok;
-        ok = mbar_wait(&bar[W_SC1], gph) && ok;  // every T1 ancestor's entries are in
-        if (two) {
-            tc_fence_after();
-            // ancestors in T2: lanes 128 + quad * 32 + lane, chunks 4 + quad .. 7
-            scatter(128 + quad * 32 + lane, 4 + quad, 4, tmem, tmem + 128);
-        }
-        tc_fence_before();
-        mbar_arrive(&bar[W_SC2]);
-        ok = mbar_wait(&bar[W_SC2], gph) && ok;  // every X and Y entry is in, the Gram columns are free
-        gph ^= 1;
-        }  // !same_kh
-
-        // ---- 3. S0 part, V, P rows --------------------------------------------
-        if (tid == 0) {
-            tc_fence_after();
+        };
+        // W_t = K_t S0^T into columns 128 t
+        auto issue_w = [&]() {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t bs = smem_desc(smem_u32(sm + OFF_S0 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (t == 1 && !two) break;
-                    const uint32_t kadr = smem_u32(sm + OFF_K + (ks >> 2) * 32768 + t * 16384 + (ks & 3) * 32);
-                    const uint32_t qadr = smem_u32(sm + OFF_Q + (ks >> 2) * 32768 + t * 16384 + (ks & 3) * 32);
-                    mma_bf16(tmem + t * 256, smem_desc(kadr, 16, 1024, 2), bs, id_n128, ks > 0);        // W_t
-                    mma_bf16(tmem + t * 256 + 128, smem_desc(qadr, 16, 1024, 2), bs, id_n128, ks > 0);  // Z_t
-                }
+                mma_bf16(tmem, kdesc(OFF_K, ks), sdesc(ks), id_n128, ks > 0);
+                if (two) mma_bf16(tmem + 128, kdesc(OFF_K + 16384, ks), sdesc(ks), id_n128, ks > 0);
             }
-            mma_commit(&bar[W_S0]);
-            ok = mbar_wait(&bar[W_S0], ph) && ok;
-            // V of both tiles into the K space
+        };
+        // V of both tiles into the Q space, once the Q products are done
+        auto issue_v = [&]() {
+            ok = mbar_wait(&bar[W_G2], ph) && ok;
             const int nb1 = min(nb, 4), nb2 = nb - nb1;
             mbar_arrive_expect_tx(&bar[W_V], (uint32_t)(2 * nb * 4096));
             for (int h = 0; h < 2; ++h) {
                 for (int r = 0; r < nb1; ++r)
-                    tma_load_3d(sm + OFF_K + h * 16384 + r * 4096, &tmV, &bar[W_V], h * 64, cur.hv, cur.lo + 32 * r);
+                    tma_load_3d(sm + OFF_Q + h * 16384 + r * 4096, &tmV, &bar[W_V], h * 64, cur.hv, cur.lo + 32 * r);
                 for (int r = 0; r < nb2; ++r)
-                    tma_load_3d(sm + OFF_K + 32768 + h * 16384 + r * 4096, &tmV, &bar[W_V], h * 64, cur.hv,
+                    tma_load_3d(sm + OFF_Q + 32768 + h * 16384 + r * 4096, &tmV, &bar[W_V], h * 64, cur.hv,
                                 cur.lo + 128 + 32 * r);
             }
+        };
+        if (!same_kh) {  // block-uniform
+            if (tid == 0) {
+                ok = mbar_wait(&bar[W_K], ph) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t a = kdesc(OFF_K, ks);
+                    // K_T1 K^T (N = 256: the B operand spans both tiles' rows)
+                    mma_bf16(tmem, a, smem_desc(smem_u32(sm + OFF_K + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2),
+                             id_n256, ks > 0);
+                }
+                ok = mbar_wait(&bar[W_Q], ph) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)  // K_T1 Q^T
+                    mma_bf16(tmem + 256, kdesc(OFF_K, ks), kdesc(OFF_Q, ks), id_n256, ks > 0);
+                mma_commit(&bar[W_G1]);
+            }
+            ok = mbar_wait(&bar[W_G1], gph) && ok;
+            tc_fence_after();
+            // ancestors in T1: lanes quad * 32 + lane, chunks quad .. 7 of all 256 columns
+            scatter(quad * 32 + lane, quad, 0, tmem, tmem + 256);
+            tc_fence_before();
+            mbar_arrive(&bar[W_SC1]);
+            if (tid == 0) {
+                ok = mbar_wait(&bar[W_SC1], gph) && ok;  // the first Gram has been read out
+                tc_fence_after();
+                issue_z();
+                if (two) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t a = kdesc(OFF_K + 16384, ks);
+                        mma_bf16(tmem, a, a, id_n128, ks > 0);                                 // K_T2 K_T2^T
+                        mma_bf16(tmem + 128, a, kdesc(OFF_Q + 16384, ks), id_n128, ks > 0);   // K_T2 Q_T2^T
+                    }
+                }
+                mma_commit(&bar[W_G2]);
+                issue_v();
+            }
+            ok = mbar_wait(&bar[W_G2], ph) && ok;
+            ok = mbar_wait(&bar[W_SC1], gph) && ok;  // every T1 ancestor's entries are in
+            if (two) {
+                tc_fence_after();
+                // ancestors in T2: lanes 128 + quad * 32 + lane, chunks 4 + quad .. 7
+                scatter(128 + quad * 32 + lane, 4 + quad, 4, tmem, tmem + 128);
+            }
+            tc_fence_before();
+            mbar_arrive(&bar[W_SC2]);
+            ok = mbar_wait(&bar[W_SC2], gph) && ok;  // every X and Y entry is in, the Gram columns are free
+            gph ^= 1;
+            if (tid == 0) {
+                tc_fence_after();
+                issue_w();
+                mma_commit(&bar[W_S0M]);
+            }
+        } else if (tid == 0) {
+            ok = mbar_wait(&bar[W_K], ph) && ok;
+            ok = mbar_wait(&bar[W_Q], ph) && ok;
+            tc_fence_after();
+            issue_z();
+            mma_commit(&bar[W_G2]);
+            issue_w();
+            mma_commit(&bar[W_S0M]);
+            issue_v();
         }
+
+        // ---- 3. P rows, right-hand side, output products ----------------------
         float P[kMaxDepth];
         {
 #pragma unroll
@@ -434,10 +495,14 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
             for (int l = 0; l < kMaxDepth; ++l) P[l] = l < myd ? P[l] * (expf(gi - gam[node_at[l]]) * inv) : 0.f;
         }
-        // P rows (A operands, K-major) once the S0 MMAs have read the Q and S0 spaces
-        ok = mbar_wait(&bar[W_S0], ph) && ok;
+        if (pre_next) {
+            graw_n[i] = gr_n;
+            graw_n[4 * kNW + i] = br_n;
+        }
+        // P rows (A operands, K-major) once W is done with the K and S0 spaces
+        ok = mbar_wait(&bar[W_S0M], ph) && ok;
         {
-            uint8_t *pa = sm + (i < 128 ? OFF_Q : OFF_Q + 32768);  // P11 row i or P21 row i - 128
+            uint8_t *pa = sm + (i < 128 ? OFF_K : OFF_K + 32768);  // P11 row i or P21 row i - 128
             uint8_t *pb = sm + OFF_S0;                             // P22 row i - 128
             if (i < 128 || two) {
 #pragma unroll
@@ -457,13 +522,12 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_offset(rr, j & 127)) = __float2bfloat16_rn(P[l]);
                 }
         }
-
-        // ---- 4. right-hand side, output, epilogue -----------------------------
         // R[j][n] = beta_j v[j][n] - beta_j e^gamma_j W[j][n] over V (same MN-major
         // layout); a row with a non-finite entry, and every row past the tree, is zero
         const int tile = i >> 7;
-        uint8_t *vbuf = sm + OFF_K + tile * 32768;
-        const uint32_t wcol = tmem + (uint32_t)(tile * 256);
+        uint8_t *vbuf = sm + OFF_Q + tile * 32768;
+        const uint32_t wcol = tmem + (uint32_t)(tile * 128);
+        const uint32_t zcol = tmem + 256 + (uint32_t)(tile * 128);
         const bool live = tile == 0 || two;  // the thread's tile takes part
         ok = mbar_wait(&bar[W_V], ph) && ok;
         tc_fence_after();
@@ -508,25 +572,32 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (tid == 0) {
             // Z_T1 += P11 R_T1; Z_T2 += P21 R_T1 + P22 R_T2
             tc_fence_after();
-            const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t asub = (ks >> 2) * 16384 + (ks & 3) * 32;
-                const uint64_t r1 = smem_desc(smem_u32(sm + OFF_K + ks * 2048), 16384, 1024, 2);
-                mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_Q + asub), 16, 1024, 2), r1, id_out, true);
+                const uint64_t r1 = smem_desc(smem_u32(sm + OFF_Q + ks * 2048), 16384, 1024, 2);
+                mma_bf16(tmem + 256, smem_desc(smem_u32(sm + OFF_K + asub), 16, 1024, 2), r1, id_out, true);
                 if (two) {
-                    const uint64_t r2 = smem_desc(smem_u32(sm + OFF_K + 32768 + ks * 2048), 16384, 1024, 2);
-                    mma_bf16(tmem + 384, smem_desc(smem_u32(sm + OFF_Q + 32768 + asub), 16, 1024, 2), r1, id_out, true);
+                    const uint64_t r2 = smem_desc(smem_u32(sm + OFF_Q + 32768 + ks * 2048), 16384, 1024, 2);
+                    mma_bf16(tmem + 384, smem_desc(smem_u32(sm + OFF_K + 32768 + asub), 16, 1024, 2), r1, id_out, true);
                     mma_bf16(tmem + 384, smem_desc(smem_u32(sm + OFF_S0 + asub), 16, 1024, 2), r2, id_out, true);
                 }
             }
             mma_commit(&bar[W_OUT]);
         }
+        if (pre_next) decay_sums(graw_n);  // the next item's g of every node is in
+        if (tid == 0) {
+            ok = mbar_wait(&bar[W_OUT], ph) && ok;
+            // the K space is free: the next item's state tile, during the epilogue
+            if (more) issue_state(p, nx, sm, &bar[W_S0F]);
+        }
         ok = mbar_wait(&bar[W_OUT], ph) && ok;
         tc_fence_after();
-        // epilogue: o[i][n] = scale * e^gamma'_i * Z[i][n], NaN for a poisoned row.
-        // bf16 rows of whole 32-node boxes are staged over R in the box layout and
-        // leave by TMA; rows of a ragged last box, and fp32 rows, are stored directly.
+
+        // ---- 4. epilogue ------------------------------------------------------
+        // o[i][n] = scale * e^gamma'_i * Z[i][n], NaN for a poisoned row.  bf16 rows
+        // of whole 32-node boxes are staged over R in the box layout and leave by
+        // TMA; rows of a ragged last box, and fp32 rows, are stored directly.
         const int nt = tile == 0 ? min(n, 128) : max(n - 128, 0);  // rows of this tile
         const int nfull = nt & ~31;
         if (live) {
@@ -538,7 +609,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t zr[32];
-                tmem_ld32_nowait(wcol + 128 + lane_base + cc * 32, zr);
+                tmem_ld32_nowait(zcol + lane_base + cc * 32, zr);
                 tmem_wait_ld_into(zr);
                 float z[32];
 #pragma unroll
@@ -562,22 +633,23 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 }
             }
         }
-        fence_proxy_async_smem();  // staged rows are visible to the TMA engine
+        // each warp stores its own box of 32 staged rows (both 64-column halves)
+        // as soon as it is written
+        if (sizeof(Tout) == 2 && item_good && live && 32 * quad < nfull) {  // warp-uniform
+            fence_proxy_async_smem();  // staged rows are visible to the TMA engine
+            __syncwarp();
+            if (lane == 0) {
+                for (int h = 0; h < 2; ++h)
+                    tma_store_3d(&tmO, vbuf + h * 16384 + quad * 4096, h * 64, cur.hv, cur.lo + tile * 128 + 32 * quad);
+                bulk_commit();
+                bulk_wait_read();  // the Q space may be loaded again
+            }
+        }
         tc_fence_before();
         __syncthreads();
-        if (tid == 0 && sizeof(Tout) == 2 && item_good) {
-            const int f1 = min(n, 128) & ~31, f2 = max(n - 128, 0) & ~31;
-            for (int h = 0; h < 2; ++h) {
-                for (int r = 0; r < (f1 >> 5); ++r)
-                    tma_store_3d(&tmO, sm + OFF_K + h * 16384 + r * 4096, h * 64, cur.hv, cur.lo + 32 * r);
-                for (int r = 0; r < (f2 >> 5); ++r)
-                    tma_store_3d(&tmO, sm + OFF_K + 32768 + h * 16384 + r * 4096, h * 64, cur.hv, cur.lo + 128 + 32 * r);
-            }
-            bulk_commit();
-            bulk_wait_read();  // the K space may be loaded again
-        }
-        __syncthreads();
+        if (tid == 0 && more) issue_tokens(&tmQ, nx, sm + OFF_Q, &bar[W_Q]);
         if (!more) break;
+        convert_state(nx);  // its leading wait orders every thread after the epilogue
         cur = nx;
     }
     if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
