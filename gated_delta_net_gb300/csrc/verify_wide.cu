@@ -207,6 +207,9 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         issue_tokens(&tmQ, cur, sm + OFF_Q, &bar[W_Q]);
     }
     convert_state(cur);
+    // the item after the current one is looked up one item ahead, off the critical path
+    Item nx;
+    bool more = find_item(p, cur.idx + 1, end, tid == 0, nx);
 
     int prev_b = -1, prev_hk = -1, gph = 0;
     for (int it = 0;; ++it) {
@@ -217,8 +220,6 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const bool same_kh = same_req && cur.hk == prev_hk;  // raw X and Y rows kept too
         prev_b = cur.b;
         prev_hk = cur.hk;
-        Item nx;
-        const bool more = find_item(p, cur.idx + 1, end, tid == 0, nx);
         // per-head node data (g, beta, decay sums) of this item, and of the next one
         // when it is another value head of the same request (made during this item)
         float *graw = fbase + ph * 5 * kNW;
@@ -319,26 +320,26 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         // (its nodes i) x (word c of their ancestor rows), by five rounds of
         // shuffles (block transpose of Hacker's Delight, section 7-3, on bit-
         // reversed words so that bit c stands for column c); zero for c > w.
-        uint32_t mine[kWords];
+        if (!same_req) {  // block-uniform
+            uint32_t mine[kWords];
 #pragma unroll
-        for (int c = 0; c < kWords; ++c) {
-            mine[c] = 0u;
-            if (c > warp || same_req) continue;  // warp-uniform
-            uint32_t x = __brev(mw[c]);
-            uint32_t m = 0x0000FFFFu;
+            for (int c = 0; c < kWords; ++c) {
+                mine[c] = 0u;
+                if (c > warp) continue;  // warp-uniform
+                uint32_t x = __brev(mw[c]);
+                uint32_t m = 0x0000FFFFu;
 #pragma unroll
-            for (int j = 16; j != 0; j >>= 1, m ^= (m << j)) {
-                const uint32_t other = __shfl_xor_sync(0xffffffffu, x, j);
-                x = (lane & j) ? x ^ (((other ^ (x >> j)) & m) << j) : x ^ ((x ^ (other >> j)) & m);
+                for (int j = 16; j != 0; j >>= 1, m ^= (m << j)) {
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, x, j);
+                    x = (lane & j) ? x ^ (((other ^ (x >> j)) & m) << j) : x ^ ((x ^ (other >> j)) & m);
+                }
+                mine[c] = __brev(x);
             }
-            mine[c] = __brev(x);
-        }
-        __syncthreads();  // every ancestor row has been read by the validation
-        if (!same_req) {
+            __syncthreads();  // every ancestor row has been read by the validation
 #pragma unroll
             for (int c = 0; c < kWords; ++c) msk[(c * 32 + lane) * kWords + warp] = mine[c];
+            __syncthreads();
         }
-        __syncthreads();
         const bool item_good = *s_err == 0;
         if (i == 0 && !item_good && !same_req) flag(p.status, *s_err);
 
@@ -499,6 +500,8 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             graw_n[i] = gr_n;
             graw_n[4 * kNW + i] = br_n;
         }
+        Item nn;
+        const bool more_n = more && find_item(p, nx.idx + 1, end, tid == 0, nn);
         // P rows (A operands, K-major) once W is done with the K and S0 spaces
         ok = mbar_wait(&bar[W_S0M], ph) && ok;
         {
@@ -651,6 +654,8 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (!more) break;
         convert_state(nx);  // its leading wait orders every thread after the epilogue
         cur = nx;
+        nx = nn;
+        more = more_n;
     }
     if (!ok) flag(p.status, GDN_DEV_TIMEOUT);
     tc_fence_before();
