@@ -117,6 +117,12 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
                  : "memory");
 }
 
+// Fetch a tensor map (a kernel parameter or constant) into the TMA unit's
+// descriptor cache ahead of its first use.
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Hint: pull one box of a tensor map into L2 ahead of its load.
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"

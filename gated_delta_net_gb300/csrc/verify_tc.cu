@@ -243,6 +243,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         griddep_wait();
         return;
     }
+    // the tensor maps' descriptors, ahead of their first use
+    if (tid == 0) {
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmO);
+    }
     const int unit_end = (int)(((int64_t)(blockIdx.x + 1) * p.units) / gridDim.x);
     Unit cur;
     if (!find_unit(p, (int)(((int64_t)blockIdx.x * p.units) / gridDim.x), unit_end, tid == 0, cur)) {
@@ -327,6 +334,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             }
         };
 
+        // the first unit's K and Q: a tree-warp thread issues them, since the first
+        // TMA loads of a launch take long to issue and the aux warps meanwhile
+        // build the first unit's tree data and state tiles
+        if (tid == 32) issue_kq(cur);
         for (int it = 0;; ++it) {
             const int ph = it & 1;
             const uint32_t gram = tmem + (uint32_t)(ph * 256);
@@ -717,7 +728,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             named_sync(4, 128);
             mbar_arrive(&bar[B_DESC]);
         };
-        if (lead) issue_kq(cur);
         float gb[4];
         load_gb(cur, gb);
         meta(cur, 0, true, gb);

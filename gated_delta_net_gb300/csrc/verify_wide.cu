@@ -45,30 +45,47 @@ namespace {
 using namespace sm100;
 using namespace tiles;
 
-constexpr int kT = 256;           // threads per block = node slots
-constexpr int kNW = 256;          // nodes (two tiles of 128)
-constexpr int kMaxDepth = 16;
 constexpr float kGammaFloor = -80.f;
-constexpr int kXS = 20;           // row stride (floats) of the raw X and Y rows
-constexpr int kWords = 8;         // mask words per node
 
-// shared-memory layout (bytes from the dynamic base, which is 1024-aligned)
-constexpr int OFF_K = 0;          // K [2 k-blocks][256 rows][128 B]; then P11 (+0) and P21 (+32 KB); then the next S0 (fp32)
-constexpr int OFF_Q = 65536;      // Q [2 k-blocks][256 rows][128 B]; then V|R|outputs of T1 (+0) and T2 (+32 KB)
-constexpr int OFF_S0 = 131072;    // S0 bf16 [2 k-blocks][128][128 B]; then P22
-constexpr int OFF_X = 163840;     // float [256][kXS] raw k.k of strict ancestors
-constexpr int OFF_Y = OFF_X + kNW * kXS * 4;            // float [256][kXS] raw q.k of ancestors
-constexpr int OFF_MASK = OFF_Y + kNW * kXS * 4;         // uint32 [256][8] ancestor, then descendant rows
-constexpr int OFF_PATH = OFF_MASK + kNW * kWords * 4;   // uint8 [256][16]
-constexpr int OFF_F = OFF_PATH + kNW * kMaxDepth;       // float [2 items][graw, gam, egt, eg, bet][256]
-constexpr int OFF_I = OFF_F + 2 * 5 * kNW * 4;          // int dep, par [256]
-constexpr int OFF_MISC = OFF_I + 2 * kNW * 4;           // tmem slot; pset[8]; err
-constexpr int OFF_BAR = OFF_MISC + 64;
+// Block shape and shared-memory layout (bytes from the dynamic base, which is
+// 1024-aligned) for NT node tiles of 128 and paths of at most MAXD nodes:
+// NT = 2, MAXD = 16 for trees of up to 256 nodes; NT = 1, MAXD = 32 for trees of
+// up to 128 nodes deeper than the one-tile kernel of verify_tc.cu takes.
+template <int NT, int MAXD>
+struct Cfg {
+    static constexpr int kT = 128 * NT;     // threads per block = node slots
+    static constexpr int kNW = 128 * NT;    // nodes
+    static constexpr int kMaxDepth = MAXD;
+    static constexpr int kXS = MAXD + 4;    // row stride (floats) of the raw X and Y rows
+    static constexpr int kWords = 4 * NT;   // mask words per node
+    static constexpr int kKB = kNW * 128;   // bytes of one 64-column k-block of K or Q
+    // K [2 k-blocks][kNW rows][128 B]; then P11 (+0) and P21 (+32 KB)
+    static constexpr int OFF_K = 0;
+    // Q [2 k-blocks][kNW rows][128 B]; then V|R|outputs of T1 (+0) and T2 (+32 KB)
+    static constexpr int OFF_Q = 2 * kKB;
+    // S0 bf16 [2 k-blocks][128][128 B]; then P22
+    static constexpr int OFF_S0 = 4 * kKB;
+    // the next item's fp32 state tile: in the K space once the output products
+    // are done (two tiles), else a region of its own, free for the whole item
+    static constexpr bool kOwnStage = NT == 1;
+    static constexpr int OFF_STG = kOwnStage ? OFF_S0 + 32768 : OFF_K;
+    static constexpr int OFF_X = kOwnStage ? OFF_STG + 65536 : OFF_S0 + 32768;  // float [kNW][kXS] raw k.k of strict ancestors
+    static constexpr int OFF_Y = OFF_X + kNW * kXS * 4;            // float [kNW][kXS] raw q.k of ancestors
+    static constexpr int OFF_MASK = OFF_Y + kNW * kXS * 4;         // uint32 [kNW][kWords] ancestor, then descendant rows
+    static constexpr int OFF_PATH = OFF_MASK + kNW * kWords * 4;   // uint8 [kNW][MAXD]
+    static constexpr int OFF_F = OFF_PATH + kNW * MAXD;            // float [2 items][graw, gam, egt, eg, bet][kNW]
+    static constexpr int OFF_I = OFF_F + 2 * 5 * kNW * 4;          // int dep, par [kNW]
+    static constexpr int OFF_MISC = OFF_I + 2 * kNW * 4;           // tmem slot; pset[8]; err
+    static constexpr int OFF_BAR = OFF_MISC + 64;
+    static constexpr int kSmemBytes = OFF_BAR + 11 * 8;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(MAXD % 16 == 0, "path rows are read 16 bytes at a time");
+};
 // K, Q arrived; first Gram done, scattered; Q products done (the Q space is
 // free); second scatter; W done (the K and S0 spaces are free); V arrived;
 // output products done; next state tile arrived; wait probe
 enum { W_K, W_Q, W_G1, W_SC1, W_G2, W_SC2, W_S0M, W_V, W_OUT, W_S0F, W_PROBE, W_BARS };
-constexpr int kSmemBytes = OFF_BAR + W_BARS * 8;
+static_assert(W_BARS == 11, "barrier count in Cfg");
 
 struct WideParams {
     int hk_n, hv_n, words, stride, total, items;
@@ -87,14 +104,14 @@ struct Item {
 
 // The first item in [idx, end) whose request is non-empty and well placed;
 // others are flagged (when `report`) and passed over.
-__device__ bool find_item(const WideParams &p, int idx, int end, bool report, Item &it) {
+__device__ bool find_item(const WideParams &p, int idx, int end, int max_n, bool report, Item &it) {
     for (; idx < end; ++idx) {
         const int b = idx / p.hv_n;
         const int lo = __ldg(p.offsets + b);
         const int n = __ldg(p.offsets + b + 1) - lo;
         if (n == 0) continue;
-        if (n > kNW || lo < 0 || lo + n > p.total) {
-            if (report) flag(p.status, n > kNW ? GDN_DEV_TOO_MANY : GDN_DEV_BAD_DESC);
+        if (n > max_n || lo < 0 || lo + n > p.total) {
+            if (report) flag(p.status, n > max_n ? GDN_DEV_TOO_MANY : GDN_DEV_BAD_DESC);
             continue;
         }
         it.idx = idx;
@@ -108,25 +125,32 @@ __device__ bool find_item(const WideParams &p, int idx, int end, bool report, It
     return false;
 }
 
-// Thread 0: the item's fp32 state tile (64 KB, contiguous) into the K space.
-__device__ __forceinline__ void issue_state(const WideParams &p, const Item &it, uint8_t *sm, uint64_t *bar) {
+// Thread 0: the item's fp32 state tile (64 KB, contiguous) into `dst`.
+__device__ __forceinline__ void issue_state(const WideParams &p, const Item &it, uint8_t *dst, uint64_t *bar) {
     const uint8_t *src = reinterpret_cast<const uint8_t *>(p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD));
     mbar_arrive_expect_tx(bar, 65536u);
-    for (int c = 0; c < 4; ++c) bulk_load(sm + OFF_K + c * 16384, src + c * 16384, 16384u, bar);
+    for (int c = 0; c < 4; ++c) bulk_load(dst + c * 16384, src + c * 16384, 16384u, bar);
 }
 
-// Thread 0: the item's K or Q rows (boxes of 32 nodes, both 64-column halves).
-__device__ __forceinline__ void issue_tokens(const CUtensorMap *map, const Item &it, uint8_t *dst, uint64_t *bar) {
+// Thread 0: the item's K or Q rows (boxes of 32 nodes, both 64-column halves,
+// k-blocks `kb_bytes` apart).
+__device__ __forceinline__ void issue_tokens(const CUtensorMap *map, const Item &it, uint8_t *dst, uint64_t *bar,
+                                             int kb_bytes) {
     const int nb = (it.n + 31) >> 5;
     mbar_arrive_expect_tx(bar, (uint32_t)(2 * nb * 4096));
     for (int kb = 0; kb < 2; ++kb)
-        for (int r = 0; r < nb; ++r) tma_load_3d(dst + kb * 32768 + r * 4096, map, bar, kb * 64, it.hk, it.lo + 32 * r);
+        for (int r = 0; r < nb; ++r) tma_load_3d(dst + kb * kb_bytes + r * 4096, map, bar, kb * 64, it.hk, it.lo + 32 * r);
 }
 
-template <typename Tout>
-__global__ void __launch_bounds__(kT, 1)
+template <typename Tout, int NT, int MAXD>
+__global__ void __launch_bounds__(128 * NT, 1)
 verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, WideParams p) {
+    using C = Cfg<NT, MAXD>;
+    constexpr int kT = C::kT, kNW = C::kNW, kMaxDepth = C::kMaxDepth, kXS = C::kXS, kWords = C::kWords, kKB = C::kKB;
+    constexpr int OFF_K = C::OFF_K, OFF_Q = C::OFF_Q, OFF_S0 = C::OFF_S0, OFF_STG = C::OFF_STG, OFF_X = C::OFF_X,
+                  OFF_Y = C::OFF_Y, OFF_MASK = C::OFF_MASK, OFF_PATH = C::OFF_PATH, OFF_F = C::OFF_F, OFF_I = C::OFF_I,
+                  OFF_MISC = C::OFF_MISC, OFF_BAR = C::OFF_BAR;
     extern __shared__ __align__(1024) uint8_t sm[];
     float *Xs = reinterpret_cast<float *>(sm + OFF_X);
     float *Ys = reinterpret_cast<float *>(sm + OFF_Y);
@@ -151,7 +175,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     // head follow each other and share the tree data, the Gram and its scatter
     const int end = (int)(((int64_t)(blockIdx.x + 1) * p.items) / gridDim.x);
     Item cur;
-    if (!find_item(p, (int)(((int64_t)blockIdx.x * p.items) / gridDim.x), end, tid == 0, cur)) {
+    if (!find_item(p, (int)(((int64_t)blockIdx.x * p.items) / gridDim.x), end, kNW, tid == 0, cur)) {
         griddep_wait();  // the block ends after the preceding grid, like the others
         return;
     }
@@ -174,48 +198,54 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     if (p.probe > 0 && tid == 0) ok = mbar_wait(&bar[W_PROBE], 0, (uint32_t)p.probe);
     griddep_wait();  // S0 may be the output of a preceding grid
 
-    const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
+    const uint32_t id_nw = idesc_bf16_f32(128, kNW), id_n128 = idesc_bf16_f32(128, 128);
     const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
 
-    // The fp32 state tile in the K space to bf16 in the S0 space (B operand,
-    // K-major, 128-byte swizzle): rows 16 warp .. 16 warp + 15, lane l holds
-    // columns 4l .. 4l + 3; then the K space takes the item's keys.
+    // The fp32 state tile in the staging space to bf16 in the S0 space (B
+    // operand, K-major, 128-byte swizzle): rows 16 warp .. 16 warp + 15, and 64
+    // rows further on too with one tile's four warps; lane l holds columns
+    // 4l .. 4l + 3;
+    // then, with two tiles, the K space takes the item's keys.
     int sph = 0;
     auto convert_state = [&](const Item &it) {
         ok = mbar_wait(&bar[W_S0F], sph) && ok;
         sph ^= 1;
-        float4 sa[8], sb[8];
-        const float4 *src = reinterpret_cast<const float4 *>(sm + OFF_K);
+        const float4 *src = reinterpret_cast<const float4 *>(sm + OFF_STG);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            sa[r] = src[(warp * 16 + r) * 32 + lane];
-            sb[r] = src[(warp * 16 + 8 + r) * 32 + lane];
-        }
+        for (int r0 = warp * 16; r0 < kD; r0 += kT / 2) {  // 16 rows per warp and pass
+            float4 sa[8], sb[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + r, 4 * lane)) =
-                make_uint2(pack_bf16(sa[r].x, sa[r].y), pack_bf16(sa[r].z, sa[r].w));
-            *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(warp * 16 + 8 + r, 4 * lane)) =
-                make_uint2(pack_bf16(sb[r].x, sb[r].y), pack_bf16(sb[r].z, sb[r].w));
+            for (int r = 0; r < 8; ++r) {
+                sa[r] = src[(r0 + r) * 32 + lane];
+                sb[r] = src[(r0 + 8 + r) * 32 + lane];
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(r0 + r, 4 * lane)) =
+                    make_uint2(pack_bf16(sa[r].x, sa[r].y), pack_bf16(sa[r].z, sa[r].w));
+                *reinterpret_cast<uint2 *>(sm + OFF_S0 + sw128_offset(r0 + 8 + r, 4 * lane)) =
+                    make_uint2(pack_bf16(sb[r].x, sb[r].y), pack_bf16(sb[r].z, sb[r].w));
+            }
         }
-        fence_proxy_async_smem();  // the bf16 tile is read, the K space written, by the async proxy
+        fence_proxy_async_smem();  // the bf16 tile is read, the staging space written, by the async proxy
         __syncthreads();
-        if (tid == 0) issue_tokens(&tmK, it, sm + OFF_K, &bar[W_K]);
+        if (tid == 0 && !C::kOwnStage) issue_tokens(&tmK, it, sm + OFF_K, &bar[W_K], kKB);
     };
     if (tid == 0) {
-        issue_state(p, cur, sm, &bar[W_S0F]);
-        issue_tokens(&tmQ, cur, sm + OFF_Q, &bar[W_Q]);
+        issue_state(p, cur, sm + OFF_STG, &bar[W_S0F]);
+        issue_tokens(&tmQ, cur, sm + OFF_Q, &bar[W_Q], kKB);
+        if (C::kOwnStage) issue_tokens(&tmK, cur, sm + OFF_K, &bar[W_K], kKB);
     }
     convert_state(cur);
     // the item after the current one is looked up one item ahead, off the critical path
     Item nx;
-    bool more = find_item(p, cur.idx + 1, end, tid == 0, nx);
+    bool more = find_item(p, cur.idx + 1, end, kNW, tid == 0, nx);
 
     int prev_b = -1, prev_hk = -1, gph = 0;
     for (int it = 0;; ++it) {
         const int ph = it & 1;
         const int n = cur.n, nb = (n + 31) >> 5;
-        const bool two = n > 128;  // block-uniform: the second tile has nodes
+        const bool two = NT == 2 && n > 128;  // block-uniform: the second tile has nodes
         const bool same_req = cur.b == prev_b;               // tree data kept
         const bool same_kh = same_req && cur.hk == prev_hk;  // raw X and Y rows kept too
         prev_b = cur.b;
@@ -226,6 +256,8 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         float *gam = graw + kNW, *egt = graw + 2 * kNW, *eg = graw + 3 * kNW, *bet = graw + 4 * kNW;
         float *graw_n = fbase + (ph ^ 1) * 5 * kNW;
         const bool pre_next = more && nx.b == cur.b;
+        // with a staging region of its own, the next state tile loads during the whole item
+        if (C::kOwnStage && tid == 0 && more) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
         float gr_n = 0.f, br_n = 0.f;  // in flight during the item
         if (pre_next && i < n) {
             gr_n = __ldg(p.g + (int64_t)(nx.lo + i) * p.hv_n + nx.hv);
@@ -299,11 +331,13 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         // node i's path (i itself past the depth, so every index stays in range)
         const int myd = i < n ? min(max(dep[i], 0), kMaxDepth) : 0;
         int node_at[kMaxDepth];
-        {
-            const uint4 pr = *reinterpret_cast<const uint4 *>(path + i * kMaxDepth);
+#pragma unroll
+        for (int h = 0; h < kMaxDepth / 16; ++h) {
+            const uint4 pr = reinterpret_cast<const uint4 *>(path + i * kMaxDepth)[h];
             const uint32_t pw[4] = {pr.x, pr.y, pr.z, pr.w};
 #pragma unroll
-            for (int l = 0; l < kMaxDepth; ++l) node_at[l] = l < myd ? (int)((pw[l >> 2] >> (8 * (l & 3))) & 0xFFu) : i;
+            for (int l = 16 * h; l < 16 * h + 16; ++l)
+                node_at[l] = l < myd ? (int)((pw[(l >> 2) & 3] >> (8 * (l & 3))) & 0xFFu) : i;
         }
         // decay sums along the path (made by the previous item for the same request)
         auto decay_sums = [&](float *f) {
@@ -351,7 +385,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         auto scatter = [&](int a, int cc0, int org, uint32_t kk, uint32_t kq) {
             const int da = a < n ? min(max(dep[a], 1), kMaxDepth) : 1;
 #pragma unroll 1
-            for (int cc = cc0 + grp; cc < kWords; cc += 2) {
+            for (int cc = cc0 + grp; cc < kWords; cc += NT) {
                 const uint32_t dm = msk[a * kWords + cc];
                 if (!__any_sync(0xffffffffu, dm != 0u)) continue;
                 uint32_t v[32];
@@ -370,7 +404,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         };
         // k-step ks of a 128-row operand at `base` (two 16 KB k-blocks per 128 rows)
         auto kdesc = [&](int off, int ks) {
-            return smem_desc(smem_u32(sm + off + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2);
+            return smem_desc(smem_u32(sm + off + (ks >> 2) * kKB + (ks & 3) * 32), 16, 1024, 2);
         };
         auto sdesc = [&](int ks) {  // S0 bf16: 128 rows, k-blocks of 16 KB
             return smem_desc(smem_u32(sm + OFF_S0 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
@@ -411,15 +445,14 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t a = kdesc(OFF_K, ks);
-                    // K_T1 K^T (N = 256: the B operand spans both tiles' rows)
-                    mma_bf16(tmem, a, smem_desc(smem_u32(sm + OFF_K + (ks >> 2) * 32768 + (ks & 3) * 32), 16, 1024, 2),
-                             id_n256, ks > 0);
+                    // K_T1 K^T (N = kNW: the B operand spans every tile's rows)
+                    mma_bf16(tmem, a, a, id_nw, ks > 0);
                 }
                 ok = mbar_wait(&bar[W_Q], ph) && ok;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // K_T1 Q^T
-                    mma_bf16(tmem + 256, kdesc(OFF_K, ks), kdesc(OFF_Q, ks), id_n256, ks > 0);
+                    mma_bf16(tmem + 256, kdesc(OFF_K, ks), kdesc(OFF_Q, ks), id_nw, ks > 0);
                 mma_commit(&bar[W_G1]);
             }
             ok = mbar_wait(&bar[W_G1], gph) && ok;
@@ -474,7 +507,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         float P[kMaxDepth];
         {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kMaxDepth / 4; ++q) {
                 const float4 y = reinterpret_cast<const float4 *>(Ys + i * kXS)[q];
                 P[4 * q] = y.x; P[4 * q + 1] = y.y; P[4 * q + 2] = y.z; P[4 * q + 3] = y.w;
             }
@@ -501,7 +534,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             graw_n[4 * kNW + i] = br_n;
         }
         Item nn;
-        const bool more_n = more && find_item(p, nx.idx + 1, end, tid == 0, nn);
+        const bool more_n = more && find_item(p, nx.idx + 1, end, kNW, tid == 0, nn);
         // P rows (A operands, K-major) once W is done with the K and S0 spaces
         ok = mbar_wait(&bar[W_S0M], ph) && ok;
         {
@@ -591,8 +624,10 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (pre_next) decay_sums(graw_n);  // the next item's g of every node is in
         if (tid == 0) {
             ok = mbar_wait(&bar[W_OUT], ph) && ok;
-            // the K space is free: the next item's state tile, during the epilogue
-            if (more) issue_state(p, nx, sm, &bar[W_S0F]);
+            // the K space is free: the next item's state tile (two tiles) or its
+            // keys (one tile), during the epilogue
+            if (more && !C::kOwnStage) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
+            if (more && C::kOwnStage) issue_tokens(&tmK, nx, sm + OFF_K, &bar[W_K], kKB);
         }
         ok = mbar_wait(&bar[W_OUT], ph) && ok;
         tc_fence_after();
@@ -650,7 +685,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         tc_fence_before();
         __syncthreads();
-        if (tid == 0 && more) issue_tokens(&tmQ, nx, sm + OFF_Q, &bar[W_Q]);
+        if (tid == 0 && more) issue_tokens(&tmQ, nx, sm + OFF_Q, &bar[W_Q], kKB);
         if (!more) break;
         convert_state(nx);  // its leading wait orders every thread after the epilogue
         cur = nx;
@@ -663,13 +698,42 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// One launch shape: NT node tiles, paths of at most MAXD nodes.
+template <int NT, int MAXD>
+cudaError_t launch_shape(const gdn_verify_args &a, cudaStream_t stream, bool after_commit, const CUtensorMap &tmK,
+                         const CUtensorMap &tmQ, const CUtensorMap &tmV, const CUtensorMap &tmO, WideParams p) {
+    using C = Cfg<NT, MAXD>;
+    p.words = a.mask_words < C::kWords ? a.mask_words : C::kWords;
+    static int have_bf16[16], have_f32[16];
+    auto kern = a.out_dtype == GDN_BF16 ? verify_wide_kernel<__nv_bfloat16, NT, MAXD> : verify_wide_kernel<float, NT, MAXD>;
+    cudaError_t e = ensure_smem(kern, C::kSmemBytes, a.out_dtype == GDN_BF16 ? have_bf16 : have_f32);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    // persistent: one block per SM (it takes all 512 tensor-memory columns)
+    cfg.gridDim = dim3((unsigned)std::min(p.items, sm_count()));
+    cfg.blockDim = dim3(C::kT);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    // after a commit of the state in the same stream, the launch may begin while
+    // the commit drains (the kernel waits for it before its first state read)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = after_commit ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmK, tmQ, tmV, tmO, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
 
+// Two tiles (paths of up to 16 nodes) for trees of 129 to 256 nodes; one tile
+// with paths of up to 32 nodes for smaller trees.
 bool verify_wide_supported(const gdn_verify_args &a) {
-    return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && a.max_nodes <= kNW &&
-           a.max_depth >= 1 && a.max_depth <= kMaxDepth && a.total_nodes > 0 && tiles::aligned16(a.q) &&
-           tiles::aligned16(a.k) && tiles::aligned16(a.v) && tiles::aligned16(a.S0) && tiles::aligned16(a.o) &&
-           tensor_map_encoder() != nullptr;
+    const bool shape = a.max_nodes > 128 ? a.max_nodes <= 256 && a.max_depth <= 16 : a.max_depth <= 32;
+    return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && shape && a.max_depth >= 1 &&
+           a.total_nodes > 0 && tiles::aligned16(a.q) && tiles::aligned16(a.k) && tiles::aligned16(a.v) &&
+           tiles::aligned16(a.S0) && tiles::aligned16(a.o) && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_verify_wide(const gdn_verify_args &a, cudaStream_t stream, bool after_commit) {
@@ -684,31 +748,14 @@ cudaError_t launch_verify_wide(const gdn_verify_args &a, cudaStream_t stream, bo
         tmO = tmV;  // unused by the fp32-output kernel
     }
     WideParams p;
-    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.words = a.mask_words < kWords ? a.mask_words : kWords;
+    p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.words = 0;
     p.stride = a.mask_words; p.probe = wait_probe_polls();
     p.total = a.total_nodes; p.items = a.batch * a.n_v_heads; p.scale = a.scale;
     p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth; p.mask = a.anc_mask;
     p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
     p.o = a.o; p.status = a.dev_status;
-    static int have_bf16[16], have_f32[16];
-    auto kern = a.out_dtype == GDN_BF16 ? verify_wide_kernel<__nv_bfloat16> : verify_wide_kernel<float>;
-    cudaError_t e = ensure_smem(kern, kSmemBytes, a.out_dtype == GDN_BF16 ? have_bf16 : have_f32);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    // persistent: one block per SM (it takes all 512 tensor-memory columns)
-    cfg.gridDim = dim3((unsigned)std::min(p.items, sm_count()));
-    cfg.blockDim = dim3(kT);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    // after a commit of the state in the same stream, the launch may begin while
-    // the commit drains (the kernel waits for it before its first state read)
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = after_commit ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tmK, tmQ, tmV, tmO, p);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return a.max_nodes > 128 ? launch_shape<2, 16>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p)
+                             : launch_shape<1, 32>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p);
 }
 
 }  // namespace gdn

@@ -186,10 +186,12 @@ typedef struct {
  *     (I + X) U = beta * (V - exp(gamma) * K S0^T)
  *     O = scale * (exp(gamma) * Q S0^T + Y U)
  * S0 is read, never written.  Nodes off a node's path never affect its output.
- * Fast paths: bf16 q/k/v with d_k = d_v = 128 and 1 <= max_depth <= 16 run a
- * tcgen05/TMA kernel, one node tile per request for max_nodes <= 128 and two
- * for 128 < max_nodes <= 256 (a deeper tree sets GDN_DEV_TOO_DEEP and its
- * request is skipped); every other case runs the general kernel, which
+ * Fast paths: bf16 q/k/v with d_k = d_v = 128 run a tcgen05/TMA kernel when
+ * the declared max_depth is 1..16 (max_nodes <= 128: one node tile per
+ * request, two value heads at a time; 128 < max_nodes <= 256: two node tiles)
+ * or 17..32 with max_nodes <= 128 (one tile, one value head at a time).  A
+ * tree deeper than the declared max_depth sets GDN_DEV_TOO_DEEP and its
+ * request is skipped.  Every other case runs the general kernel, which
  * accepts any depth.
  * q and k need no normalisation on any path (the fast paths keep the raw
  * products k_i.k_j and q_i.k_j in fp32); non-finite inputs propagate to the

@@ -255,3 +255,123 @@ def test_wide_commit_verify_serving_order():
     assert st == 0
     new.S0 = S_ref.astype(np.float32)
     assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
+
+
+# ----------------------------------------------------------------------------
+# one tile, paths of 17 to 32 nodes (declared max_depth 17..32, N <= 128)
+# ----------------------------------------------------------------------------
+
+def _deep_tree(rng, n, cap):
+    """Mostly chain-like: node i hangs under node i - 1 with probability 3/4
+    (while that node is shallower than `cap`), else under a random node of
+    depth < cap; paths reach the cap."""
+    parent = np.full(n, -1, np.int32)
+    depth = np.ones(n, np.int32)
+    for i in range(1, n):
+        if depth[i - 1] < cap and rng.random() < 0.75:
+            parent[i] = i - 1
+        else:
+            open_nodes = np.flatnonzero(depth[:i] < cap)
+            parent[i] = rng.choice(open_nodes) if open_nodes.size else -1
+        depth[i] = 1 if parent[i] < 0 else depth[parent[i]] + 1
+    return parent
+
+
+def _deep_batch(seed, sizes, depth=32, hk=2, hv=4, fn=None):
+    tb = _batch(seed, sizes, hk=hk, hv=hv, fn=fn or (lambda r, n: _deep_tree(r, n, depth)))
+    tb.max_depth_bound = depth
+    return tb
+
+
+@pytest.mark.parametrize("sizes", [(128,), (128, 40, 1, 0, 77), (33, 32, 31, 128, 2)])
+def test_deep_sizes(sizes):
+    tb = _deep_batch(sum(sizes) + 7, sizes)
+    depth = np.ones(tb.total_nodes, np.int64)
+    for b in range(tb.batch):
+        lo = tb.node_offsets[b]
+        for i in range(tb.node_offsets[b + 1] - lo):
+            a = tb.parent[lo + i]
+            depth[lo + i] = 1 if a < 0 else depth[lo + a] + 1
+    if max(sizes) >= 64:
+        assert depth.max() > 16            # the paths go past the two-head kernel's bound
+    o, status, _ = _verify(tb, max_depth=32)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_deep_chains_and_general_kernel():
+    # chains of 32 and 20 nodes and a random tree: paths up to the declared bound
+    chains = {32: W.chain_tree(32), 20: W.chain_tree(20)}
+    tb = _deep_batch(31, (32, 20, 128), fn=lambda r, n: chains[n] if n in chains else _deep_tree(r, n, 32))
+    o, st, d = _verify(tb, max_depth=32)
+    gb.check_status(st)
+    o_gen, st2, _ = _verify(tb, d=d, max_depth=0)
+    gb.check_status(st2)
+    ref = oracle.verify(tb)
+    assert _rel(o.float().cpu().numpy(), ref) <= TOL_BF16
+    assert _rel(o_gen.float().cpu().numpy(), ref) <= TOL_BF16
+
+
+def test_deep_tree_beyond_the_bound_is_flagged():
+    tb = _deep_batch(32, (40, 30), fn=lambda r, n: W.chain_tree(n))
+    out = torch.full((tb.total_nodes, tb.n_v_heads, tb.d_v), 7.0, dtype=torch.bfloat16, device="cuda")
+    _, status, _ = _verify(tb, max_depth=32, out=out)
+    assert int(status.item()) & DEV_TOO_DEEP
+    assert torch.all(out[:40] == 7.0)          # the 40-deep chain is skipped
+    assert _rel(out[40:].float().cpu().numpy(), oracle.verify(tb)[40:]) <= TOL_BF16
+
+
+def test_deep_shallow_trees_under_a_deep_bound():
+    # trees of depth <= 16 declared with max_depth 32 take the one-tile kernel
+    tb = _batch(33, (128, 64, 100))
+    tb.max_depth_bound = 32
+    o, status, _ = _verify(tb, max_depth=32)
+    gb.check_status(status)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_deep_fp32_output_many_items_and_S0_untouched():
+    sizes = tuple((0, 1, 33, 128, 7, 100, 2, 128)[i % 8] for i in range(120))
+    tb = _deep_batch(34, sizes)
+    tb.scale = 0.5
+    d = gb.upload(tb)
+    before = d["S0"].clone()
+    o, status, _ = _verify(tb, d=d, max_depth=32, out_dtype=torch.float32)
+    gb.check_status(status)
+    assert o.dtype == torch.float32
+    assert torch.equal(before, d["S0"])
+    assert _rel(o.cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+
+
+def test_deep_non_finite_inputs_stay_on_their_branch():
+    rng = np.random.default_rng(35)
+    parent = _deep_tree(rng, 128, 32)
+    base_tb = _deep_batch(35, (128,), hk=1, hv=2, fn=lambda r, n: parent)
+    base, st, _ = _verify(base_tb, max_depth=32)
+    gb.check_status(st)
+    for bad_node in (0, 9, 100):
+        sub = {bad_node}
+        for i in range(128):
+            if parent[i] in sub:
+                sub.add(i)
+        keep = [i for i in range(128) if i not in sub]
+        tb2 = _deep_batch(35, (128,), hk=1, hv=2, fn=lambda r, n: parent)
+        tb2.k[bad_node] = np.nan
+        tb2.v[bad_node] = np.inf
+        o2, st2, _ = _verify(tb2, max_depth=32)
+        gb.check_status(st2)
+        assert torch.equal(o2[keep], base[keep])
+
+
+def test_deep_wait_probe_times_out_and_returns():
+    tb = _deep_batch(36, (128, 50, 128))
+    o0, st, d = _verify(tb, max_depth=32)
+    gb.check_status(st)
+    try:
+        gb.gdn_test_set_wait_probe(2000)
+        o1, st1, _ = _verify(tb, d=d, max_depth=32)
+        bits = int(st1.item())
+    finally:
+        gb.gdn_test_set_wait_probe(0)
+    assert bits == 16
+    assert torch.equal(o1, o0)
