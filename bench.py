@@ -268,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
     gb.lib()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    tb = bench_workload(args)
     d = gb.upload(tb, device=dev)
     T = tb.total_nodes
     words = max(1, (tb.max_nodes + 31) // 32)
@@ -523,7 +523,8 @@ def workload_config(tb, args, world) -> dict:
     """The workload both arms report (the same keys for the GPU arm and the
     oracle's reference arm)."""
     return {"workload": tb.name, "batch": tb.batch, "tree_size": args.tree_size,
-            "tree": "random parent over nodes of depth < 16 (depth <= 16)",
+            "tree": ("random parent over nodes of depth < 16 (depth <= 16)" if tb.max_depth_bound <= 16 else
+                     f"chain-like: parent i - 1 with probability 3/4, else random (depth <= {tb.max_depth_bound})"),
             "n_k_heads": tb.n_k_heads, "n_v_heads": tb.n_v_heads, "d_k": tb.d_k,
             "d_v": tb.d_v, "qkv": "bf16", "state": "fp32",
             "step": "build_desc + verify + commit",
@@ -546,6 +547,14 @@ def graph_capturer(stream):
     return capture
 
 
+def bench_workload(args):
+    """The timed workload: the serving point (trees of depth <= 16), or with
+    --depth D > 16 chain-like trees whose paths reach D nodes."""
+    if args.depth > 16:
+        return W.deep_serving(batch=args.batch, n=args.tree_size, max_depth=args.depth)
+    return W.serving_target(batch=args.batch, n=args.tree_size)
+
+
 def dominant_kernel(tb) -> str:
     """The verify kernel the library dispatches to (rule of include/gdn_tree.h)."""
     if TC_READY and tb.qkv_dtype == "bf16" and tb.d_k == 128 and tb.d_v == 128:
@@ -565,7 +574,7 @@ def run_reference(args, rank, world):
     """The float64 CPU oracle on the same workload and metric (rank 0 only)."""
     if rank != 0:
         return None
-    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    tb = bench_workload(args)
     vals, ts = [], []
     import oracle
     oracle.build()
@@ -743,7 +752,7 @@ def run_helpers(args):
     gbuild.build()
     gb.lib()
     dev = torch.device("cuda", 0)
-    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    tb = bench_workload(args)
     rng = np.random.default_rng(5)
     offs = tb.node_offsets.astype(np.int32)
     shuffled = np.empty(tb.total_nodes, np.int32)
@@ -868,6 +877,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--tree-size", type=int, default=128)
+    ap.add_argument("--depth", type=int, default=16,
+                    help="declared tree depth; above 16, chain-like trees whose paths reach it")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)

@@ -160,6 +160,22 @@ def best_first_tree(rng: np.random.Generator, n: int,
     return np.asarray(parent, dtype=np.int32)
 
 
+def chainy_tree(rng: np.random.Generator, n: int, max_depth: int) -> np.ndarray:
+    """Long paths: node i hangs under node i - 1 with probability 3/4 while that
+    node is shallower than max_depth, else under a uniform node of depth
+    < max_depth (node 0 is the root)."""
+    parent = np.full(n, -1, dtype=np.int32)
+    depth = np.ones(n, dtype=np.int32)
+    for i in range(1, n):
+        if depth[i - 1] < max_depth and rng.random() < 0.75:
+            parent[i] = i - 1
+        else:
+            open_nodes = np.flatnonzero(depth[:i] < max_depth)
+            parent[i] = int(rng.choice(open_nodes))
+        depth[i] = depth[parent[i]] + 1
+    return parent
+
+
 def chain_tree(n: int) -> np.ndarray:
     return np.arange(-1, n - 1, dtype=np.int32)
 
@@ -307,6 +323,17 @@ def serving_target(seed: int = 3, batch: int = 64, n: int = 128) -> TreeBatch:
     """The throughput point: batch 64, tree size 128 for every request, otherwise
     as ``ragged_serving``."""
     return ragged_serving(seed, batch, fixed_n=n, name=f"serving_b{batch}_n{n}")
+
+
+def deep_serving(seed: int = 6, batch: int = 64, n: int = 128, max_depth: int = 32) -> TreeBatch:
+    """Deep trees at the serving shapes: batch 64, tree size n, chain-like trees
+    whose paths reach past 16 nodes (declared bound max_depth), 16 key / 32
+    value heads, d = 128, bf16 q/k/v, fp32 state; accepted path = a uniformly
+    chosen root-to-leaf path."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(batch + 1)[-1]))
+    parents = [chainy_tree(rng, n, max_depth) for _ in range(batch)]
+    return make_batch(f"deep_b{batch}_n{n}_d{max_depth}", seed, parents, 16, 32, 128, 128, "bf16",
+                      path_random_leaf, max_depth_bound=max_depth)
 
 
 SWEEP_N = (8, 16, 32, 64, 128, 256)
