@@ -1,5 +1,5 @@
 // commit_tc.cu -- delayed state commit on the tensor cores: bf16 k/v, d_k = d_v = 128,
-// accepted paths of at most 16 nodes (sm_103a).
+// accepted paths of at most 32 nodes (sm_103a).
 //
 // "Trees from Marginals" (gist.science Technical Summary, section 3, Solution,
 // last bullet): the state is committed in the next iteration along the accepted
@@ -16,10 +16,10 @@
 // next item's path data (keys, values, g, beta, node ids and their checks) is
 // prepared into a second buffer while thread 0 waits for the current state
 // tile's store, and the next tile is requested into L2.
-// Both contractions are GEMMs with a 16-wide side and run on tcgen05 with fp32
-// accumulation:
-//     W  = S0 K^T      M = 128 state rows, N = 16 path keys, K = 128
-//     U  = A K         M = 128 state rows, N = 128 columns,  K = 16 path keys
+// Both contractions are GEMMs with a side as wide as the longest path (16, or 32
+// for longer paths) and run on tcgen05 with fp32 accumulation:
+//     W  = S0 K^T      M = 128 state rows, N = P path keys, K = 128
+//     U  = A K         M = 128 state rows, N = 128 columns, K = P path keys
 // where A[row][t] = e^(gamma_L - gamma_t) u_t[row].  The fp32 operands S0 and
 // A enter as bf16 hi + lo pairs (x = hi + lo to ~2^-17 relative) and the keys
 // are exact in bf16, so both products keep fp32 accuracy.  The chain solve for
@@ -37,22 +37,30 @@ using namespace sm100;
 
 constexpr int kT = 256;
 constexpr int kD = 128;
-constexpr int kMaxPath = 16;
-
-// shared memory (bytes from a 1024-aligned base)
-constexpr int OFF_TILE = 0;        // fp32 state tile (TMA, 4 x [128][32], 128B swizzle); also
-                                   // S0 hi | lo as bf16 K-major tiles ([2][128][128 B] each)
-// path data is double-buffered: one item's is prepared while the previous item's
-// state tile is stored
-constexpr int OFF_KEYS = 65536;    // [2] bf16 path keys [16][128], 128B swizzle (2 column blocks), 4 KB each
-constexpr int OFF_A = OFF_KEYS + 8192;  // A hi | lo: bf16 [128][16] core-matrix layout, 4 KB each
-constexpr int OFF_VP = OFF_A + 8192;    // [2] fp32 path values [16][128]
-constexpr int OFF_COEF = OFF_VP + 2 * kMaxPath * kD * 4;  // fp32 [16][16]
-constexpr int OFF_SCAL = OFF_COEF + kMaxPath * kMaxPath * 4;  // [2] bet, egam, fdec, gam [16]; pn [16]
-constexpr int kScal = 5 * kMaxPath;                           // floats per buffer
-constexpr int OFF_MISC = OFF_SCAL + 2 * kScal * 4;            // tmem slot, bad path flags [2]
-constexpr int OFF_BAR = OFF_MISC + 16;
-constexpr int kSmemBytes = OFF_BAR + 4 * 8;  // barriers: tile, W, U, probe (never arrived on)
+// Shared memory (bytes from a 1024-aligned base) for paths of at most P nodes.
+// Path data is double-buffered for P = 16 (one item's is prepared while the
+// previous item's state tile is stored); for P = 32 one buffer keeps two
+// blocks per SM (an item's path data is only prepared once the previous item's
+// products are done, so one buffer serves as well).
+template <int P>
+struct CommitCfg {
+    static constexpr int kMaxPath = P;
+    static constexpr int kBufs = P == 16 ? 2 : 1;
+    static constexpr int kKeyBytes = P * kD * 2;        // bf16 path keys [P][128], 128B swizzle (2 column blocks)
+    static constexpr int kABytes = kD * P * 2;          // A hi or lo: bf16 [128][P] core-matrix layout
+    static constexpr int OFF_TILE = 0;                  // fp32 state tile (TMA, 4 x [128][32], 128B swizzle); also
+                                                        // S0 hi | lo as bf16 K-major tiles ([2][128][128 B] each)
+    static constexpr int OFF_KEYS = 65536;              // [kBufs] path keys
+    static constexpr int OFF_A = OFF_KEYS + kBufs * kKeyBytes;  // A hi | lo
+    static constexpr int OFF_VP = OFF_A + 2 * kABytes;  // [kBufs] fp32 path values [P][128]
+    static constexpr int OFF_COEF = OFF_VP + kBufs * P * kD * 4;  // fp32 [P][P]
+    static constexpr int OFF_SCAL = OFF_COEF + P * P * 4;       // [kBufs] bet, egam, fdec, gam [P]; pn [P]
+    static constexpr int kScal = 5 * P;                         // floats per buffer
+    static constexpr int OFF_MISC = OFF_SCAL + kBufs * kScal * 4;  // tmem slot, bad path flags [2]
+    static constexpr int OFF_BAR = OFF_MISC + 16;
+    static constexpr int kSmemBytes = OFF_BAR + 4 * 8;  // barriers: tile, W, U, probe (never arrived on)
+    static_assert(2 * kSmemBytes + 2048 <= 233472, "two blocks per SM");
+};
 
 struct TcCommitParams {
     int hk_n, hv_n, total, items, batch, words;
@@ -104,11 +112,16 @@ __device__ __forceinline__ int nth_bit(const uint32_t (&m)[kMaxWords], int words
 
 // kSel = false: item (request, value head) commits the request's accepted path
 // into S_new.  kSel = true: item (selection s, value head) writes the state at
-// node sel_node[s] of request sel_req[s] into row block s of S_sel.
-template <bool kSel>
+// node sel_node[s] of request sel_req[s] into row block s of S_sel.  Paths of at
+// most P nodes.
+template <bool kSel, int P>
 __global__ void __launch_bounds__(kT, 2)
 commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmSN,
                  TcCommitParams p) {
+    using C = CommitCfg<P>;
+    constexpr int kMaxPath = C::kMaxPath, kScal = C::kScal;
+    constexpr int OFF_TILE = C::OFF_TILE, OFF_KEYS = C::OFF_KEYS, OFF_A = C::OFF_A, OFF_VP = C::OFF_VP,
+                  OFF_COEF = C::OFF_COEF, OFF_SCAL = C::OFF_SCAL, OFF_MISC = C::OFF_MISC, OFF_BAR = C::OFF_BAR;
     extern __shared__ __align__(1024) uint8_t sm[];
     float *tile = reinterpret_cast<float *>(sm + OFF_TILE);
     float *coef = reinterpret_cast<float *>(sm + OFF_COEF);
@@ -200,45 +213,48 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     // checked root first along parent -> child edges (and, for a selected node,
     // ending at it), node ids, keys (bf16, 16-byte pieces, rows past L zero),
     // values (fp32), raw g and beta.
-    auto prep = [&](const Itm &q, const uint32_t (&mrow)[kMaxWords], int buf) {
+    auto prep = [&](const Itm &q, const uint32_t (&mrow)[kMaxWords], int buf, int pb) {
         float *bet = reinterpret_cast<float *>(sm + OFF_SCAL) + buf * kScal, *gam = bet + 3 * kMaxPath;
         int *pn = reinterpret_cast<int *>(bet + 4 * kMaxPath);
         float *vp = reinterpret_cast<float *>(sm + OFF_VP) + buf * (kMaxPath * kD);
-        uint8_t *keys = sm + OFF_KEYS + buf * 4096;
+        uint8_t *keys = sm + OFF_KEYS + buf * C::kKeyBytes;
         auto node_at = [&](int t) -> int {
             if constexpr (kSel) return nth_bit(mrow, p.words, t);
             else return __ldg(p.pidx + q.pa + t);
         };
-        if (kSel && q.L == 0 && tid == 0) atomicOr(s_bad + buf, 1);
+        if (kSel && q.L == 0 && tid == 0) atomicOr(s_bad + pb, 1);
         if (tid < q.L) {
             const int node = node_at(tid);
             const int expect = tid == 0 ? -1 : node_at(tid - 1);
             pn[tid] = node;
             const bool in = node >= 0 && node < q.n;
             if (!in || __ldg(p.parent + q.lo + node) != expect || (kSel && tid == q.L - 1 && node != q.sel))
-                atomicOr(s_bad + buf, 1);
+                atomicOr(s_bad + pb, 1);
             if (in) {
                 gam[tid] = __ldg(p.g + (int64_t)(q.lo + node) * p.hv_n + q.hv);
                 bet[tid] = __ldg(p.beta + (int64_t)(q.lo + node) * p.hv_n + q.hv);
             }
         }
-        const int t = tid >> 4, c = tid & 15;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-        if (t < q.L) {
-            const int node = node_at(t);
-            if (node >= 0 && node < q.n) {
-                const int64_t gnode = q.lo + node;
-                kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (gnode * p.hk_n + q.hk) * kD) + c);
-                vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (gnode * p.hv_n + q.hv) * kD) + c);
-            }
-        }
-        *reinterpret_cast<uint4 *>(keys + sw128(t, c * 8, kMaxPath)) = kv;
-        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
-        float *vrow = vp + t * kD + c * 8;
+        const int c = tid & 15;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            vrow[2 * e] = __uint_as_float(w[e] << 16);
-            vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        for (int t = tid >> 4; t < kMaxPath; t += kT / 16) {
+            uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+            if (t < q.L) {
+                const int node = node_at(t);
+                if (node >= 0 && node < q.n) {
+                    const int64_t gnode = q.lo + node;
+                    kv = __ldg(reinterpret_cast<const uint4 *>(p.k + (gnode * p.hk_n + q.hk) * kD) + c);
+                    vv = __ldg(reinterpret_cast<const uint4 *>(p.v + (gnode * p.hv_n + q.hv) * kD) + c);
+                }
+            }
+            *reinterpret_cast<uint4 *>(keys + sw128(t, c * 8, kMaxPath)) = kv;
+            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+            float *vrow = vp + t * kD + c * 8;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                vrow[2 * e] = __uint_as_float(w[e] << 16);
+                vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
         }
     };
 
@@ -251,7 +267,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             if (tid == 0) flag(p.status, err);
             continue;
         }
-        const int L = q.L, buf = it & 1;
+        const int L = q.L, buf = C::kBufs == 2 ? (it & 1) : 0, pb = it & 1;  // data buffer; bad-flag slot
         const int row_in = (q.b * p.hv_n + q.hv) * kD, tile_row = idx * kD;
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar[0], kD * kD * 4);
@@ -263,14 +279,14 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
                     prefetch_l2(p.S0 + ((int64_t)nb * p.hv_n + nx % p.hv_n) * (kD * kD), kD * kD * 4);
             }
         }
-        if (prepped != idx) prep(q, mrow, buf);
+        if (prepped != idx) prep(q, mrow, buf, pb);
         __syncthreads();
-        const bool bad = s_bad[buf] != 0;
-        if (tid == 0) s_bad[buf ^ 1] = 0;  // the next item's flag starts clear
+        const bool bad = s_bad[pb] != 0;
+        if (tid == 0) s_bad[pb ^ 1] = 0;  // the next item's flag starts clear
         float *bet = reinterpret_cast<float *>(sm + OFF_SCAL) + buf * kScal, *egam = bet + kMaxPath,
               *fdec = bet + 2 * kMaxPath, *gam = bet + 3 * kMaxPath;
         const float *vp = reinterpret_cast<const float *>(sm + OFF_VP) + buf * (kMaxPath * kD);
-        uint8_t *keys = sm + OFF_KEYS + buf * 4096;
+        uint8_t *keys = sm + OFF_KEYS + buf * C::kKeyBytes;
         if (tid == 0 && !bad) {
             float acc = 0.f;
             for (int t = 0; t < L; ++t) {
@@ -329,16 +345,16 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
         __syncthreads();
 
         if (!bad) {
-            // W = S0 K^T (hi + lo) -> tensor-memory columns [0, 16)
+            // W = S0 K^T (hi + lo) -> tensor-memory columns [0, P)
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t id = idesc_bf16_f32(128, 16);
+                const uint32_t id = idesc_bf16_f32(128, kMaxPath);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t ad = smem_desc(smem_u32(sm + OFF_TILE + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32), 16, 1024, 2);
-                        const uint64_t bd = smem_desc(smem_u32(keys + (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, 2);
+                        const uint64_t bd = smem_desc(smem_u32(keys + (ks >> 2) * (kMaxPath * 128) + (ks & 3) * 32), 16, 1024, 2);
                         mma_bf16(tmem, ad, bd, id, part > 0 || ks > 0);
                     }
                 mma_commit(&bar[1]);
@@ -346,9 +362,14 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             ok = mbar_wait(&bar[1], ph_mma & 1) && ok;
             tc_fence_after();
             // chain solve for this row: u_t, then A[row][t] = e^(gamma_L - gamma_t) u_t
-            uint32_t wr[16];
-            tmem_ld16_nowait(tmem + lane_base, wr);
-            tmem_wait_ld();
+            uint32_t wr[kMaxPath];
+            if constexpr (kMaxPath == 16) {
+                tmem_ld16_nowait(tmem + lane_base, wr);
+                tmem_wait_ld();
+            } else {
+                tmem_ld32_nowait(tmem + lane_base, wr);
+                tmem_wait_ld_into(wr);
+            }
             float a[kMaxPath];
 #pragma unroll
             for (int t = 0; t < kMaxPath; ++t) {
@@ -369,22 +390,28 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
                 const float h = __bfloat162float(__float2bfloat16_rn(a[t]));
                 part[t] = half == 0 ? h : a[t] - h;
             }
-            uint8_t *abase = sm + OFF_A + half * 4096 + (row >> 3) * 256 + (row & 7) * 16;
+            uint8_t *abase = sm + OFF_A + half * C::kABytes + (row >> 3) * (kMaxPath * 16) + (row & 7) * 16;
 #pragma unroll
-            for (int kh = 0; kh < 2; ++kh)
+            for (int kh = 0; kh < kMaxPath / 8; ++kh)
                 *reinterpret_cast<uint4 *>(abase + kh * 128) =
                     make_uint4(pack_bf16(part[kh * 8 + 0], part[kh * 8 + 1]), pack_bf16(part[kh * 8 + 2], part[kh * 8 + 3]),
                                pack_bf16(part[kh * 8 + 4], part[kh * 8 + 5]), pack_bf16(part[kh * 8 + 6], part[kh * 8 + 7]));
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
-            // U = A K (hi + lo) -> columns [128, 256); K is the same key tile read MN-major
+            // U = A K (hi + lo) -> columns [128, 256); K is the same key tile read
+            // MN-major, 16 path keys per MMA
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16_f32(128, 128) | (1u << 16);
-                const uint64_t bd = smem_desc(smem_u32(keys), 2048, 1024, 2);
-                mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A), 128, 256, 0), bd, id, false);
-                mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A + 4096), 128, 256, 0), bd, id, true);
+#pragma unroll
+                for (int ks = 0; ks < kMaxPath / 16; ++ks) {
+                    const uint64_t bd = smem_desc(smem_u32(keys + ks * 2048), kMaxPath * 128, 1024, 2);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+                        mma_bf16(tmem + 128, smem_desc(smem_u32(sm + OFF_A + part * C::kABytes + ks * 256), 128, kMaxPath * 16, 0),
+                                 bd, id, part > 0 || ks > 0);
+                }
                 mma_commit(&bar[2]);
             }
             ok = mbar_wait(&bar[2], ph_mma & 1) && ok;
@@ -429,7 +456,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             uint32_t nm[kMaxWords];
             int nerr;
             if (params(nidx, nq, nm, nerr)) {
-                prep(nq, nm, buf ^ 1);
+                prep(nq, nm, C::kBufs == 2 ? (buf ^ 1) : 0, pb ^ 1);
                 prepped = nidx;
             }
         }
@@ -459,7 +486,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 }  // namespace
 
 bool commit_tc_supported(const gdn_commit_args &a) {
-    return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && a.max_path >= 1 && a.max_path <= kMaxPath &&
+    return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && a.max_path >= 1 && a.max_path <= 32 &&
            aligned16(a.S0) && aligned16(a.S_new) && aligned16(a.k) && aligned16(a.v) &&
            (int64_t)a.batch * a.n_v_heads * kD <= 2147483647LL && tensor_map_encoder() != nullptr;
 }
@@ -474,12 +501,19 @@ cudaError_t launch_commit_tc(const gdn_commit_args &a, cudaStream_t stream) {
     p.offsets = a.node_offsets; p.parent = a.parent; p.poff = a.path_offsets; p.pidx = a.path_idx;
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.g = a.g; p.beta = a.beta; p.status = a.dev_status; p.probe = wait_probe_polls();
-    static int have[16];
-    cudaError_t e = ensure_smem(commit_tc_kernel<false>, kSmemBytes, have);
-    if (e != cudaSuccess) return e;
-    // persistent: two blocks per SM
+    // persistent: two blocks per SM; paths of up to 16 nodes, or up to 32
     const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());
-    commit_tc_kernel<false><<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
+    if (a.max_path <= 16) {
+        static int have[16];
+        cudaError_t e = ensure_smem(commit_tc_kernel<false, 16>, CommitCfg<16>::kSmemBytes, have);
+        if (e != cudaSuccess) return e;
+        commit_tc_kernel<false, 16><<<grid, kT, CommitCfg<16>::kSmemBytes, stream>>>(tmS0, tmSN, p);
+    } else {
+        static int have[16];
+        cudaError_t e = ensure_smem(commit_tc_kernel<false, 32>, CommitCfg<32>::kSmemBytes, have);
+        if (e != cudaSuccess) return e;
+        commit_tc_kernel<false, 32><<<grid, kT, CommitCfg<32>::kSmemBytes, stream>>>(tmS0, tmSN, p);
+    }
     return cudaGetLastError();
 }
 
@@ -502,10 +536,10 @@ cudaError_t launch_states_tc(const gdn_states_args &a, cudaStream_t stream) {
     p.k = static_cast<const __nv_bfloat16 *>(a.k); p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.g = a.g; p.beta = a.beta; p.status = a.dev_status;
     static int have[16];
-    cudaError_t e = ensure_smem(commit_tc_kernel<true>, kSmemBytes, have);
+    cudaError_t e = ensure_smem(commit_tc_kernel<true, 16>, CommitCfg<16>::kSmemBytes, have);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)std::min(p.items, 2 * sm_count());
-    commit_tc_kernel<true><<<grid, kT, kSmemBytes, stream>>>(tmS0, tmSN, p);
+    commit_tc_kernel<true, 16><<<grid, kT, CommitCfg<16>::kSmemBytes, stream>>>(tmS0, tmSN, p);
     return cudaGetLastError();
 }
 

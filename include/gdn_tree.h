@@ -234,12 +234,13 @@ typedef struct {
  * S_new != S0).  A path that does not start at a root or does not follow
  * parent -> child edges sets GDN_DEV_BAD_PATH and leaves that request's S_new
  * unwritten.  Everything accumulates in fp32.
- * Fast paths for d_k = d_v = 128 and 1 <= max_path <= 16: bf16 k/v run a
+ * Fast paths for d_k = d_v = 128: bf16 k/v with 1 <= max_path <= 32 run a
  * persistent tcgen05 kernel (two blocks per SM walking the (request, value
  * head) items, the state tile moved by TMA both ways); fp32 k/v (and bf16
- * k/v the tensor-core kernel does not take) run one block per item with the
- * tile moved by TMA.  A longer path sets GDN_DEV_TOO_DEEP and
- * its request is skipped.  Every other case runs the general kernel.
+ * k/v the tensor-core kernel does not take) with 1 <= max_path <= 16 run one
+ * block per item with the tile moved by TMA.  A path longer than the declared
+ * max_path sets GDN_DEV_TOO_DEEP and its request is skipped.  Every other case
+ * runs the general kernel.
  */
 GDN_API int gdn_tree_commit(const gdn_commit_args *args, void *stream);
 

@@ -375,3 +375,87 @@ def test_deep_wait_probe_times_out_and_returns():
         gb.gdn_test_set_wait_probe(0)
     assert bits == 16
     assert torch.equal(o1, o0)
+
+
+# ----------------------------------------------------------------------------
+# the tensor-core commit for accepted paths of 17 to 32 nodes (max_path <= 32)
+# ----------------------------------------------------------------------------
+
+TOL_STATE = 1e-4
+
+
+def _commit(tb, d, max_path, out=None):
+    status = gb.new_status()
+    S = gb.gdn_tree_commit(d["k"], d["v"], d["g"], d["beta"], d["S0"], d["node_offsets"], d["parent"],
+                           d["path_offsets"], d["path_idx"], tb.max_nodes, max_path=max_path, out=out,
+                           dev_status=status)
+    torch.cuda.synchronize()
+    return S, status
+
+
+@pytest.mark.parametrize("path", ["leaf", "deepest", "empty", "chain32"])
+def test_long_path_commit_matches_oracle(path):
+    fns = {"leaf": W.path_random_leaf, "deepest": W.path_deepest_leaf, "empty": lambda p, r: [],
+           "chain32": W.path_whole_chain}
+    rng = np.random.default_rng(41)
+    if path == "chain32":
+        parents = [W.chain_tree(32), W.chain_tree(17), W.chain_tree(1)]
+    else:
+        parents = [_deep_tree(rng, n, 32) for n in (128, 40, 1, 77)]
+    tb = W.custom(41, parents, n_k_heads=2, n_v_heads=4, d=128, qkv_dtype="bf16", path_fn=fns[path])
+    d = gb.upload(tb)
+    S, status = _commit(tb, d, 32)
+    gb.check_status(status)
+    S_ref, st = oracle.commit(tb)
+    assert st == 0
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    # the same as the general kernel (no declared bound)
+    S_gen, status = _commit(tb, d, 0)
+    gb.check_status(status)
+    assert _rel(S_gen.cpu().numpy(), S_ref) <= TOL_STATE
+
+
+def test_long_path_commit_in_place_and_many_items():
+    rng = np.random.default_rng(42)
+    parents = [_deep_tree(rng, int(n), 32) for n in rng.integers(20, 129, 150)]
+    tb = W.custom(42, parents, n_k_heads=2, n_v_heads=4, d=128, qkv_dtype="bf16",
+                  path_fn=W.path_deepest_leaf)
+    d = gb.upload(tb)
+    S_ref, st = oracle.commit(tb)
+    assert st == 0
+    S, status = _commit(tb, d, 32, out=d["S0"])
+    gb.check_status(status)
+    assert S.data_ptr() == d["S0"].data_ptr()
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+
+
+def test_path_beyond_32_is_flagged():
+    tb = W.custom(43, [W.chain_tree(40), W.chain_tree(30)], n_k_heads=1, n_v_heads=2, d=128,
+                  qkv_dtype="bf16", path_fn=W.path_whole_chain)
+    d = gb.upload(tb)
+    sentinel = torch.full_like(d["S0"], 3.0)
+    S, status = _commit(tb, d, 32, out=sentinel)
+    assert int(status.item()) & DEV_TOO_DEEP
+    assert torch.all(sentinel[0] == 3.0)       # the 40-node path is skipped
+    S_ref, _ = oracle.commit(tb)
+    assert _rel(sentinel[1].cpu().numpy(), S_ref[1]) <= TOL_STATE
+
+
+def test_deep_commit_then_verify():
+    # serving order on deep trees: the previous tree's accepted path (up to 32
+    # nodes) committed on the tensor cores, the new tree verified from it
+    prev, new = _deep_batch(44, (128, 90)), _deep_batch(45, (128, 100))
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes,
+                                         dev_status=status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 32, dn["q"], dn["k"], dn["v"],
+                                     dn["g"], dn["beta"], dn["node_offsets"], dn["parent"], mask,
+                                     depth, new.max_nodes, max_depth=32, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    S_ref, st = oracle.commit(prev)
+    assert st == 0
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    new.S0 = S_ref.astype(np.float32)
+    assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
