@@ -474,10 +474,10 @@ def run_ours(args, rank, world, local_rank):
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        ent = tr.get(kernel)
-        if ent and ent.get("source_sha") == source_sha(KERNEL_SOURCES[kernel]) and \
-                ent.get("workload") == tb.name:
-            traffic = ent.get("dram_bytes_per_launch")
+        ents = tr.get(kernel) or []
+        for ent in ents if isinstance(ents, list) else [ents]:
+            if ent.get("source_sha") == source_sha(KERNEL_SOURCES[kernel]) and ent.get("workload") == tb.name:
+                traffic = ent.get("dram_bytes_per_launch")
     cpu_v, cpu_threads, cpu_desc, _ = oracle_sample(tb, args.cpu_seconds)
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
