@@ -305,6 +305,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
     const uint32_t id_n256 = idesc_bf16_f32(128, 256), id_n128 = idesc_bf16_f32(128, 128);
 
+    // S0 of value head g of unit u as bf16 (B operand, K-major, 128-byte
+    // swizzle) into head g's S space by one warp group; eight rows per batch,
+    // double-buffered; lane l holds columns 4l .. 4l + 3 (coalesced row reads).
+    auto convert = [&](const Unit &u, int g) {
+        const int sw = quad;  // rows 32 sw .. 32 sw + 31 of the state tile
+        const float *s0t = p.S0 + ((int64_t)u.b * p.hv_n + hv_of(u, g)) * (kD * kD);
+        uint8_t *dst = sm + OFF_S + g * 32768;
+        float4 s0a[8], s0b[8];
+        auto s0_load = [&](float4 (&d)[8], int batch) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                d[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (sw * 32 + batch * 8 + r) * kD) + lane);
+        };
+        auto s0_put = [&](const float4 (&src)[8], int batch) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                *reinterpret_cast<uint2 *>(dst + sw128_offset(sw * 32 + batch * 8 + r, 4 * lane)) =
+                    make_uint2(pack_bf16(src[r].x, src[r].y), pack_bf16(src[r].z, src[r].w));
+        };
+        s0_load(s0a, 0);
+        s0_load(s0b, 1);
+        s0_put(s0a, 0);
+        s0_load(s0a, 2);
+        s0_put(s0b, 1);
+        s0_load(s0b, 3);
+        s0_put(s0a, 2);
+        s0_put(s0b, 3);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[B_S0IN0 + g]);
+    };
+
     if (role == 0) {
         // ======================= tree warps ===================================
         const int i = tid;
@@ -375,6 +406,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             fence_proxy_async_smem();
             mbar_arrive(&bar[B_P1]);
             if (!more) break;
+            // the next unit's head-B state tile, into head B's S space, free since
+            // its S0 MMA (the aux warps convert head A's)
+            if (it == 0) griddep_wait();  // S0 may be the output of the preceding grid
+            convert(nx, 1);
             cur = nx;
         }
     } else if (role <= 2) {
@@ -572,36 +607,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         // ======================= aux warps ====================================
         const int i = tid & 127;
         const bool lead = i == 0;
-        const int sw = quad;  // rows 32 sw .. 32 sw + 31 of each state tile
-        // S0 of value head g of unit u as bf16 (B operand, K-major, 128-byte
-        // swizzle) into head g's S space; eight rows per batch, double-buffered;
-        // lane l holds columns 4l .. 4l + 3 (coalesced row reads).
-        auto convert = [&](const Unit &u, int g) {
-            const float *s0t = p.S0 + ((int64_t)u.b * p.hv_n + hv_of(u, g)) * (kD * kD);
-            uint8_t *dst = sm + OFF_S + g * 32768;
-            float4 s0a[8], s0b[8];
-            auto s0_load = [&](float4 (&d)[8], int batch) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    d[r] = __ldg(reinterpret_cast<const float4 *>(s0t + (sw * 32 + batch * 8 + r) * kD) + lane);
-            };
-            auto s0_put = [&](const float4 (&src)[8], int batch) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    *reinterpret_cast<uint2 *>(dst + sw128_offset(sw * 32 + batch * 8 + r, 4 * lane)) =
-                        make_uint2(pack_bf16(src[r].x, src[r].y), pack_bf16(src[r].z, src[r].w));
-            };
-            s0_load(s0a, 0);
-            s0_load(s0b, 1);
-            s0_put(s0a, 0);
-            s0_load(s0a, 2);
-            s0_put(s0b, 1);
-            s0_load(s0b, 3);
-            s0_put(s0a, 2);
-            s0_put(s0b, 3);
-            fence_proxy_async_smem();
-            mbar_arrive(&bar[B_S0IN0 + g]);
-        };
         // g and beta of both value heads of a unit at node i (loaded a unit ahead)
         auto load_gb = [&](const Unit &u, float (&gb)[4]) {
             gb[0] = gb[1] = gb[2] = gb[3] = 0.f;
@@ -755,9 +760,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             ok = mbar_wait(&bar[B_META1], ph) && ok;
             ok = mbar_wait(&bar[B_META2], ph) && ok;
             meta(nx, ph ^ 1, nx.meta, gb);
-            // the next unit's S0 tiles: both S spaces are free since the S0 MMAs
-#pragma unroll 1
-            for (int g = 0; g < 2; ++g) convert(nx, g);
+            // the next unit's head-A state tile (the tree warps convert head B's)
+            convert(nx, 0);
             cur = nx;
         }
     }
