@@ -562,7 +562,7 @@ def dominant_kernel(tb) -> str:
             return "verify_tc"
         if tb.max_nodes <= 256 and 1 <= tb.max_depth_bound <= 16:
             return "verify_wide"
-        if tb.max_nodes <= 128 and 1 <= tb.max_depth_bound <= 32:
+        if tb.max_nodes <= 128 and 1 <= tb.max_depth_bound <= 64:
             return "verify_wide"
     return "verify_simt"
 

@@ -49,8 +49,15 @@ constexpr float kGammaFloor = -80.f;
 
 // Block shape and shared-memory layout (bytes from the dynamic base, which is
 // 1024-aligned) for NT node tiles of 128 and paths of at most MAXD nodes:
-// NT = 2, MAXD = 16 for trees of up to 256 nodes; NT = 1, MAXD = 32 for trees of
-// up to 128 nodes deeper than the one-tile kernel of verify_tc.cu takes.
+// NT = 2, MAXD = 16 for trees of up to 256 nodes; NT = 1, MAXD = 32 or 64 for
+// trees of up to 128 nodes deeper than the one-tile kernel of verify_tc.cu takes.
+// Where the next item's fp32 state tile waits for its conversion to bf16:
+enum StageMode {
+    kStageK,       // in the K space, once the output products are done (two tiles)
+    kStageOwn,     // in a 64 KB region of its own, loading during the whole item
+    kStageDirect,  // nowhere: converted straight from global memory (paths of up to
+                   // 64 nodes leave no room for a staging region)
+};
 template <int NT, int MAXD>
 struct Cfg {
     static constexpr int kT = 128 * NT;     // threads per block = node slots
@@ -65,11 +72,9 @@ struct Cfg {
     static constexpr int OFF_Q = 2 * kKB;
     // S0 bf16 [2 k-blocks][128][128 B]; then P22
     static constexpr int OFF_S0 = 4 * kKB;
-    // the next item's fp32 state tile: in the K space once the output products
-    // are done (two tiles), else a region of its own, free for the whole item
-    static constexpr bool kOwnStage = NT == 1;
-    static constexpr int OFF_STG = kOwnStage ? OFF_S0 + 32768 : OFF_K;
-    static constexpr int OFF_X = kOwnStage ? OFF_STG + 65536 : OFF_S0 + 32768;  // float [kNW][kXS] raw k.k of strict ancestors
+    static constexpr StageMode kStage = NT == 2 ? kStageK : MAXD <= 32 ? kStageOwn : kStageDirect;
+    static constexpr int OFF_STG = kStage == kStageOwn ? OFF_S0 + 32768 : OFF_K;  // fp32 staging (unused when direct)
+    static constexpr int OFF_X = kStage == kStageOwn ? OFF_STG + 65536 : OFF_S0 + 32768;  // float [kNW][kXS] raw k.k of strict ancestors
     static constexpr int OFF_Y = OFF_X + kNW * kXS * 4;            // float [kNW][kXS] raw q.k of ancestors
     static constexpr int OFF_MASK = OFF_Y + kNW * kXS * 4;         // uint32 [kNW][kWords] ancestor, then descendant rows
     static constexpr int OFF_PATH = OFF_MASK + kNW * kWords * 4;   // uint8 [kNW][MAXD]
@@ -201,16 +206,21 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const uint32_t id_nw = idesc_bf16_f32(128, kNW), id_n128 = idesc_bf16_f32(128, 128);
     const uint32_t id_out = id_n128 | (1u << 16);  // B (R) is MN-major
 
-    // The fp32 state tile in the staging space to bf16 in the S0 space (B
+    // The fp32 state tile in the staging space (or global memory) to bf16 in the S0 space (B
     // operand, K-major, 128-byte swizzle): rows 16 warp .. 16 warp + 15, and 64
     // rows further on too with one tile's four warps; lane l holds columns
     // 4l .. 4l + 3;
     // then, with two tiles, the K space takes the item's keys.
     int sph = 0;
     auto convert_state = [&](const Item &it) {
-        ok = mbar_wait(&bar[W_S0F], sph) && ok;
-        sph ^= 1;
-        const float4 *src = reinterpret_cast<const float4 *>(sm + OFF_STG);
+        const float4 *src;
+        if constexpr (C::kStage == kStageDirect) {
+            src = reinterpret_cast<const float4 *>(p.S0 + ((int64_t)it.b * p.hv_n + it.hv) * (kD * kD));
+        } else {
+            ok = mbar_wait(&bar[W_S0F], sph) && ok;
+            sph ^= 1;
+            src = reinterpret_cast<const float4 *>(sm + OFF_STG);
+        }
 #pragma unroll
         for (int r0 = warp * 16; r0 < kD; r0 += kT / 2) {  // 16 rows per warp and pass
             float4 sa[8], sb[8];
@@ -229,12 +239,12 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         fence_proxy_async_smem();  // the bf16 tile is read, the staging space written, by the async proxy
         __syncthreads();
-        if (tid == 0 && !C::kOwnStage) issue_tokens(&tmK, it, sm + OFF_K, &bar[W_K], kKB);
+        if (tid == 0 && C::kStage == kStageK) issue_tokens(&tmK, it, sm + OFF_K, &bar[W_K], kKB);
     };
     if (tid == 0) {
-        issue_state(p, cur, sm + OFF_STG, &bar[W_S0F]);
+        if (C::kStage != kStageDirect) issue_state(p, cur, sm + OFF_STG, &bar[W_S0F]);
         issue_tokens(&tmQ, cur, sm + OFF_Q, &bar[W_Q], kKB);
-        if (C::kOwnStage) issue_tokens(&tmK, cur, sm + OFF_K, &bar[W_K], kKB);
+        if (C::kStage != kStageK) issue_tokens(&tmK, cur, sm + OFF_K, &bar[W_K], kKB);
     }
     convert_state(cur);
     // the item after the current one is looked up one item ahead, off the critical path
@@ -257,7 +267,7 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         float *graw_n = fbase + (ph ^ 1) * 5 * kNW;
         const bool pre_next = more && nx.b == cur.b;
         // with a staging region of its own, the next state tile loads during the whole item
-        if (C::kOwnStage && tid == 0 && more) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
+        if (C::kStage == kStageOwn && tid == 0 && more) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
         float gr_n = 0.f, br_n = 0.f;  // in flight during the item
         if (pre_next && i < n) {
             gr_n = __ldg(p.g + (int64_t)(nx.lo + i) * p.hv_n + nx.hv);
@@ -626,8 +636,8 @@ verify_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             ok = mbar_wait(&bar[W_OUT], ph) && ok;
             // the K space is free: the next item's state tile (two tiles) or its
             // keys (one tile), during the epilogue
-            if (more && !C::kOwnStage) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
-            if (more && C::kOwnStage) issue_tokens(&tmK, nx, sm + OFF_K, &bar[W_K], kKB);
+            if (more && C::kStage == kStageK) issue_state(p, nx, sm + OFF_STG, &bar[W_S0F]);
+            if (more && C::kStage != kStageK) issue_tokens(&tmK, nx, sm + OFF_K, &bar[W_K], kKB);
         }
         ok = mbar_wait(&bar[W_OUT], ph) && ok;
         tc_fence_after();
@@ -728,9 +738,9 @@ cudaError_t launch_shape(const gdn_verify_args &a, cudaStream_t stream, bool aft
 }  // namespace
 
 // Two tiles (paths of up to 16 nodes) for trees of 129 to 256 nodes; one tile
-// with paths of up to 32 nodes for smaller trees.
+// with paths of up to 32 or 64 nodes for smaller trees.
 bool verify_wide_supported(const gdn_verify_args &a) {
-    const bool shape = a.max_nodes > 128 ? a.max_nodes <= 256 && a.max_depth <= 16 : a.max_depth <= 32;
+    const bool shape = a.max_nodes > 128 ? a.max_nodes <= 256 && a.max_depth <= 16 : a.max_depth <= 64;
     return a.qkv_dtype == GDN_BF16 && a.d_k == kD && a.d_v == kD && shape && a.max_depth >= 1 &&
            a.total_nodes > 0 && tiles::aligned16(a.q) && tiles::aligned16(a.k) && tiles::aligned16(a.v) &&
            tiles::aligned16(a.S0) && tiles::aligned16(a.o) && tensor_map_encoder() != nullptr;
@@ -754,8 +764,9 @@ cudaError_t launch_verify_wide(const gdn_verify_args &a, cudaStream_t stream, bo
     p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth; p.mask = a.anc_mask;
     p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
     p.o = a.o; p.status = a.dev_status;
-    return a.max_nodes > 128 ? launch_shape<2, 16>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p)
-                             : launch_shape<1, 32>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p);
+    if (a.max_nodes > 128) return launch_shape<2, 16>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p);
+    if (a.max_depth <= 32) return launch_shape<1, 32>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p);
+    return launch_shape<1, 64>(a, stream, after_commit, tmK, tmQ, tmV, tmO, p);
 }
 
 }  // namespace gdn

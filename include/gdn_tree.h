@@ -189,7 +189,7 @@ typedef struct {
  * Fast paths: bf16 q/k/v with d_k = d_v = 128 run a tcgen05/TMA kernel when
  * the declared max_depth is 1..16 (max_nodes <= 128: one node tile per
  * request, two value heads at a time; 128 < max_nodes <= 256: two node tiles)
- * or 17..32 with max_nodes <= 128 (one tile, one value head at a time).  A
+ * or 17..64 with max_nodes <= 128 (one tile, one value head at a time).  A
  * tree deeper than the declared max_depth sets GDN_DEV_TOO_DEEP and its
  * request is skipped.  Every other case runs the general kernel, which
  * accepts any depth.

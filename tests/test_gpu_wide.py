@@ -459,3 +459,58 @@ def test_deep_commit_then_verify():
     assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
     new.S0 = S_ref.astype(np.float32)
     assert _rel(o.float().cpu().numpy(), oracle.verify(new)) <= TOL_BF16
+
+
+# ----------------------------------------------------------------------------
+# one tile, paths of 33 to 64 nodes (declared max_depth 33..64, N <= 128)
+# ----------------------------------------------------------------------------
+
+def test_chain64_bf16_d128():
+    # the 64-node chain at d = 128 in bf16, with a deep tree and a single node
+    chain = W.chain_tree(64)
+    tb = _deep_batch(51, (64, 128, 1), depth=64,
+                     fn=lambda r, n: chain if n == 64 else _deep_tree(r, n, 64))
+    tb.max_depth_bound = 64
+    o, status, d = _verify(tb, max_depth=64)
+    gb.check_status(status)
+    ref = oracle.verify(tb)
+    assert _rel(o.float().cpu().numpy(), ref) <= TOL_BF16
+    o_gen, st2, _ = _verify(tb, d=d, max_depth=0)
+    gb.check_status(st2)
+    assert _rel(o_gen.float().cpu().numpy(), ref) <= TOL_BF16
+
+
+def test_depth64_many_items_fp32_output_and_flag():
+    sizes = tuple((128, 0, 65, 7, 100, 1)[i % 6] for i in range(60))
+    tb = _deep_batch(52, sizes, depth=64)
+    tb.max_depth_bound = 64
+    o, status, _ = _verify(tb, max_depth=64, out_dtype=torch.float32)
+    gb.check_status(status)
+    assert _rel(o.cpu().numpy(), oracle.verify(tb)) <= TOL_BF16
+    # a 70-node chain under a declared bound of 64 is flagged and skipped
+    tb2 = _deep_batch(53, (70, 40), depth=64, fn=lambda r, n: W.chain_tree(n))
+    out = torch.full((tb2.total_nodes, tb2.n_v_heads, tb2.d_v), 7.0, dtype=torch.bfloat16, device="cuda")
+    _, status2, _ = _verify(tb2, max_depth=64, out=out)
+    assert int(status2.item()) & DEV_TOO_DEEP
+    assert torch.all(out[:70] == 7.0)
+    assert _rel(out[70:].float().cpu().numpy(), oracle.verify(tb2)[70:]) <= TOL_BF16
+
+
+def test_depth64_non_finite_inputs_stay_on_their_branch():
+    parent = W.chain_tree(64)
+    parent[40] = 20                            # a branch at node 20: 40..63 hang under it
+    base_tb = _deep_batch(54, (64,), hk=1, hv=2, depth=64, fn=lambda r, n: parent)
+    base, st, _ = _verify(base_tb, max_depth=64)
+    gb.check_status(st)
+    for bad_node in (10, 45):
+        sub = {bad_node}
+        for i in range(64):
+            if parent[i] in sub:
+                sub.add(i)
+        keep = [i for i in range(64) if i not in sub]
+        tb2 = _deep_batch(54, (64,), hk=1, hv=2, depth=64, fn=lambda r, n: parent)
+        tb2.k[bad_node] = np.nan
+        tb2.g[bad_node] = np.inf
+        o2, st2, _ = _verify(tb2, max_depth=64)
+        gb.check_status(st2)
+        assert torch.equal(o2[keep], base[keep])
