@@ -606,7 +606,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     } else {
         // ======================= aux warps ====================================
         const int i = tid & 127;
-        const bool lead = i == 0;
         // g and beta of both value heads of a unit at node i (loaded a unit ahead)
         auto load_gb = [&](const Unit &u, float (&gb)[4]) {
             gb[0] = gb[1] = gb[2] = gb[3] = 0.f;
