@@ -14,8 +14,16 @@
 //   phase 1: per node, W = S0 k, Z = S0 q for the slab, R = beta (v - e^gamma W);
 //   phase 2: per depth level, per node (one warp): dot products with each
 //            ancestor's key, forward substitution for u_i, then o_i.
+// For small trees (max_nodes x path bound <= kRawMax) the coefficients of every
+// (node, ancestor) pair, beta_i e^(gamma_i - gamma_a) k_i.k_a and
+// e^(gamma_i - gamma_a) q_i.k_a, and each node's path are made first, by all warps
+// at once (phase 1b), so that the level-ordered phase 2 only combines them: a
+// chain, one node per level, then no longer runs its dot products one level at a
+// time.
 // Only a node's ancestors are ever read, so a non-finite input on one branch
 // cannot reach another branch's outputs.  Everything accumulates in fp32.
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace gdn {
@@ -23,9 +31,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRawMax = 4096;  // entries of each raw dot-product table [nodes][path length]
 
 struct SimtParams {
     int hk_n, hv_n, dv, max_nodes, sw;
+    int md;  // > 0: phase 1b on, rows of md entries (path length bound); 0: off
     float scale;
     const int32_t *offsets, *parent, *depth;
     const void *q, *k, *v;
@@ -35,12 +45,12 @@ struct SimtParams {
 };
 
 struct SmemLayout {
-    int s0, ub, zb, gam, gl, bet, kq;  // float offsets
+    int s0, ub, zb, gam, gl, bet, kq, rk, rq, self, pth;  // float offsets (pth: int entries)
     int par, dep, order, cnt, start;   // int offsets (after the floats)
     int floats, ints;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int nm, int sw, int dk) {
+__host__ __device__ inline SmemLayout smem_layout(int nm, int sw, int dk, int md) {
     SmemLayout L;
     int f = 0;
     L.s0 = f;  f += sw * (dk + 1);
@@ -50,6 +60,10 @@ __host__ __device__ inline SmemLayout smem_layout(int nm, int sw, int dk) {
     L.gl = f;  f += nm;
     L.bet = f; f += nm;
     L.kq = f;  f += kWarps * 2 * dk;
+    L.rk = f;  f += nm * md;
+    L.rq = f;  f += nm * md;
+    L.self = f; f += md > 0 ? nm : 0;
+    L.pth = f; f += nm * md;
     L.floats = f;
     int i = 0;
     L.par = i;   i += nm;
@@ -67,8 +81,11 @@ verify_simt_kernel(SimtParams p) {
     constexpr int EPL = (DK + 31) / 32;  // key elements per lane
     extern __shared__ float smem[];
     const int nm = p.max_nodes, SW = p.sw;
-    const SmemLayout L = smem_layout(nm, SW, DK);
+    const SmemLayout L = smem_layout(nm, SW, DK, p.md);
     float *S0s = smem + L.s0, *Ub = smem + L.ub, *Zb = smem + L.zb;
+    float *RK = smem + L.rk, *RQ = smem + L.rq, *SELF = smem + L.self;  // phase 1b tables
+    int *PTH = reinterpret_cast<int *>(smem + L.pth);
+    const int MD = p.md;
     float *gam = smem + L.gam, *gl = smem + L.gl, *bet = smem + L.bet;
     int *ism = reinterpret_cast<int *>(smem + L.floats);
     int *par = ism + L.par, *dep = ism + L.dep, *order = ism + L.order;
@@ -185,10 +202,94 @@ verify_simt_kernel(SimtParams p) {
     }
     __syncthreads();
 
+    // ---- phase 1b: pair coefficients of every (node, ancestor) pair --------
+    // for the strict ancestors a of i, at l = dep(a) - 1:
+    //   RK[i][l] = beta_i e^(gamma_i - gamma_a) k_i.k_a,  RQ[i][l] = e^(gamma_i - gamma_a) q_i.k_a,
+    //   PTH[i][l] = a;  SELF[i] = q_i.k_i.  The rows hold MD >= the tree's depth entries.
+    const bool raw = MD > 0 && maxd <= MD;
+    if (raw) {
+        for (int i = warp; i < n; i += kWarps) {
+            const int64_t krow = ((int64_t)(lo + i) * p.hk_n + hk) * DK;
+            float kr[EPL], qr[EPL];
+#pragma unroll
+            for (int r = 0; r < EPL; ++r) {
+                const int m = lane + 32 * r;
+                kr[r] = m < DK ? load_f(kp, krow + m) : 0.f;
+                qr[r] = m < DK ? load_f(qp, krow + m) : 0.f;
+            }
+            float self = 0.f;
+#pragma unroll
+            for (int r = 0; r < EPL; ++r) self = fmaf(qr[r], kr[r], self);
+            self = warp_sum(self);
+            if (lane == 0) SELF[i] = self;
+            // ancestors four at a time: their key rows are requested together
+            constexpr int kBatch = 4;
+            for (int j = par[i]; j >= 0;) {
+                int js[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    js[u] = j;
+                    if (j >= 0) j = par[j];
+                }
+                float kj[kBatch][EPL];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int64_t jrow = ((int64_t)(lo + max(js[u], 0)) * p.hk_n + hk) * DK;
+#pragma unroll
+                    for (int r = 0; r < EPL; ++r) {
+                        const int m = lane + 32 * r;
+                        kj[u][r] = (js[u] >= 0 && m < DK) ? load_f(kp, jrow + m) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (js[u] < 0) break;  // warp-uniform
+                    float pk = 0.f, pq = 0.f;
+#pragma unroll
+                    for (int r = 0; r < EPL; ++r) {
+                        pk = fmaf(kr[r], kj[u][r], pk);
+                        pq = fmaf(qr[r], kj[u][r], pq);
+                    }
+                    pk = warp_sum(pk);
+                    pq = warp_sum(pq);
+                    if (lane == 0) {
+                        const int ja = js[u], l = dep[ja] - 1;
+                        const float dec = expf(gam[i] - gam[ja]);
+                        RK[i * MD + l] = bet[i] * dec * pk;
+                        RQ[i * MD + l] = dec * pq;
+                        PTH[i * MD + l] = ja;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+
     // ---- phase 2: level-ordered forward substitution and outputs ----------
     for (int d = 1; d <= maxd; ++d) {
         for (int idx = start[d] + warp; idx < start[d + 1]; idx += kWarps) {
             const int i = order[idx];
+            if (raw) {
+                // the pair coefficients are in the tables: combine along the path,
+                // from the parent up
+                const float gi = gam[i];
+                float acc_u = lane < SW ? Ub[i * SW + lane] : 0.f;
+                float acc_o = 0.f;
+                const int *pi_row = PTH + i * MD;
+                const float *rk = RK + i * MD, *rq = RQ + i * MD;
+                for (int l = dep[i] - 2; l >= 0; --l) {
+                    const int j = pi_row[l];
+                    const float uj = lane < SW ? Ub[j * SW + lane] : 0.f;
+                    acc_u -= rk[l] * uj;
+                    acc_o += rq[l] * uj;
+                }
+                if (lane < SW) {
+                    Ub[i * SW + lane] = acc_u;
+                    const float o = p.scale * (expf(gi) * Zb[i * SW + lane] + acc_o + SELF[i] * acc_u);
+                    store_f(op, ((int64_t)(lo + i) * p.hv_n + h) * p.dv + slab * SW + lane, o);
+                }
+                continue;
+            }
             const int64_t krow = ((int64_t)(lo + i) * p.hk_n + hk) * DK;
             float kr[EPL], qr[EPL];
 #pragma unroll
@@ -255,7 +356,7 @@ verify_simt_kernel(SimtParams p) {
 
 template <typename Tin, typename Tout, int DK>
 cudaError_t launch_typed(const SimtParams &p, int batch, cudaStream_t stream) {
-    const SmemLayout L = smem_layout(p.max_nodes, p.sw, DK);
+    const SmemLayout L = smem_layout(p.max_nodes, p.sw, DK, p.md);
     const size_t bytes = sizeof(float) * (size_t)L.floats + sizeof(int) * (size_t)L.ints;
     auto kern = verify_simt_kernel<Tin, Tout, DK>;
     static int have[16];  // one per template instance
@@ -283,6 +384,9 @@ cudaError_t launch_verify_simt(const gdn_verify_args &a, cudaStream_t stream) {
     SimtParams p;
     p.hk_n = a.n_k_heads; p.hv_n = a.n_v_heads; p.dv = a.d_v; p.max_nodes = a.max_nodes;
     p.sw = a.d_v < 32 ? a.d_v : 32;
+    // phase 1b for small trees: path length bound = the declared depth, else the node count
+    const int md = a.max_depth > 0 ? std::min(a.max_depth, a.max_nodes) : a.max_nodes;
+    p.md = (int64_t)a.max_nodes * md <= kRawMax ? md : 0;
     p.scale = a.scale;
     p.offsets = a.node_offsets; p.parent = a.parent; p.depth = a.depth;
     p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta; p.S0 = a.S0;
