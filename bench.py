@@ -549,10 +549,15 @@ def graph_capturer(stream):
 
 def bench_workload(args):
     """The timed workload: the serving point (trees of depth <= 16), or with
-    --depth D > 16 chain-like trees whose paths reach D nodes."""
+    --depth D > 16 chain-like trees whose paths reach D nodes, or with --depth 0
+    the serving point with no declared depth bound (the general kernels)."""
     if args.depth > 16:
         return W.deep_serving(batch=args.batch, n=args.tree_size, max_depth=args.depth)
-    return W.serving_target(batch=args.batch, n=args.tree_size)
+    tb = W.serving_target(batch=args.batch, n=args.tree_size)
+    if args.depth == 0:
+        tb.max_depth_bound = 0
+        tb.name += "_nobound"
+    return tb
 
 
 def dominant_kernel(tb) -> str:
@@ -878,7 +883,8 @@ def main():
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--tree-size", type=int, default=128)
     ap.add_argument("--depth", type=int, default=16,
-                    help="declared tree depth; above 16, chain-like trees whose paths reach it")
+                    help="declared tree depth; above 16, chain-like trees whose paths reach it; "
+                         "0, no declared bound (the general kernels)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
