@@ -105,3 +105,45 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.source_sha(["a.cu"]) == h1
     (tmp_path / "a.cu").write_text("int x = 2;\nint y;\n")
     assert bench.source_sha(["a.cu"]) != h1
+
+
+@pytest.mark.parametrize("depth,size,workload,kernel", [
+    (16, 128, "serving_b64_n128", "verify_tc"),
+    (16, 256, "serving_b64_n256", "verify_wide"),
+    (32, 128, "deep_b64_n128_d32", "verify_wide"),
+    (64, 128, "deep_b64_n128_d64", "verify_wide"),
+    (0, 128, "serving_b64_n128_nobound", "verify_simt"),
+])
+def test_bench_workload_and_kernel(depth, size, workload, kernel):
+    import argparse
+    args = argparse.Namespace(depth=depth, batch=64, tree_size=size)
+    tb = bench.bench_workload(args)
+    assert tb.name == workload
+    assert bench.dominant_kernel(tb) == kernel
+    assert tb.max_nodes == size
+    # the declared depth bound holds for every tree, and deep workloads reach past 16
+    depth_of = np.ones(tb.total_nodes, np.int64)
+    for b in range(tb.batch):
+        lo = int(tb.node_offsets[b])
+        for i in range(int(tb.node_offsets[b + 1]) - lo):
+            a = tb.parent[lo + i]
+            depth_of[lo + i] = 1 if a < 0 else depth_of[lo + a] + 1
+    if depth:
+        assert depth_of.max() <= max(depth, 16)
+    if depth > 16:
+        assert depth_of.max() > 16
+
+
+def test_traffic_entries_match_their_workloads():
+    # every recorded capture names its workload and command, and a kernel's
+    # entries are for distinct workloads
+    with open(bench.TRAFFIC_FILE) as f:
+        tr = json.load(f)
+    for kernel, ents in tr.items():
+        assert kernel in bench.KERNEL_SOURCES
+        ents = ents if isinstance(ents, list) else [ents]
+        names = [e["workload"] for e in ents]
+        assert len(names) == len(set(names))
+        for e in ents:
+            assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
+            assert e["command"].startswith("ncu ") and "--clock-control none" in e["command"]
