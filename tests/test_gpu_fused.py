@@ -175,3 +175,101 @@ def test_bad_previous_path_is_flagged_and_left_unwritten():
     assert torch.all(sentinel[1] == 3.0)             # the bad request's state is not committed
     assert not torch.all(sentinel[0] == 3.0) and not torch.all(sentinel[2] == 3.0)
     assert not torch.all(o_init[:30] == 5.0)
+
+
+# ----------------------------------------------------------------------------
+# edge cases of the chained call on the tensor-core kernels (bf16, d = 128,
+# max_path <= 16, new trees of at most 128 nodes with depth <= 16)
+# ----------------------------------------------------------------------------
+
+DEV_BAD_PATH, DEV_TOO_DEEP, DEV_TIMEOUT = 2, 8, 16
+
+
+def _trees(seed, sizes):
+    rng = np.random.default_rng(seed)
+    return [W.depth_capped_random_tree(rng, n, 16) if n > 0 else np.zeros(0, np.int32) for n in sizes]
+
+
+def test_odd_value_head_groups_in_place():
+    # 6 value heads over 2 key heads: the verification's second pair of each key
+    # head holds one head
+    prev = W.custom(41, _trees(40, [50, 70, 90]), n_k_heads=2, n_v_heads=6, d=128, qkv_dtype="bf16")
+    new = W.custom(42, _trees(43, [90, 30, 128]), n_k_heads=2, n_v_heads=6, d=128, qkv_dtype="bf16")
+    o, S, status, S0_before = _run(prev, new, in_place=True)
+    gb.check_status(status)
+    prev.S0 = S0_before.cpu().numpy()
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("batch", [6, 320])
+def test_requests_with_empty_new_trees_are_still_committed(batch):
+    # every third new tree is empty: those requests verify nothing but are still
+    # committed (batch 320: more verification units than SMs)
+    rng = np.random.default_rng(50 + batch)
+    prev_sizes = [int(rng.integers(2, 24)) for _ in range(batch)]
+    new_sizes = [0 if r % 3 == 1 else int(rng.integers(1, 24)) for r in range(batch)]
+    prev = W.custom(51, _trees(52, prev_sizes), n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16")
+    new = W.custom(53, _trees(54, new_sizes), n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16",
+                   path_fn=lambda p, r: [])
+    o, S, status, _ = _run(prev, new)
+    gb.check_status(status)
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_path_past_max_path_is_flagged_and_left_unwritten():
+    # request 0 accepts a 20-node chain against max_path = 16
+    chain = np.arange(-1, 19, dtype=np.int32)
+    tree = _trees(60, [40])[0]
+    leaf_path = W.path_random_leaf(tree, np.random.default_rng(61))
+    paths = iter([list(range(20)), leaf_path])
+    prev = W.custom(62, [chain, tree], n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16",
+                    path_fn=lambda p, r: next(paths))
+    new = W.custom(63, [tree, tree], n_k_heads=1, n_v_heads=2, d=128, qkv_dtype="bf16")
+    sentinel = torch.full((2, 2, 128, 128), 3.0, device="cuda")
+    o, S, status, _ = _run(prev, new, S_new_init=sentinel)
+    assert int(status.item()) == DEV_TOO_DEEP
+    assert torch.all(S[0] == 3.0)
+    S_ref, st = oracle.commit(prev)      # the oracle has no path bound
+    assert st == 0
+    assert _rel(S[1].cpu().numpy(), S_ref[1]) <= TOL_STATE
+    new.S0 = S_ref
+    o_ref = oracle.verify(new)
+    lo = int(new.node_offsets[1])
+    assert _rel(o[lo:].float().cpu().numpy(), o_ref[lo:]) <= TOL_BF16
+
+
+def test_fp32_outputs():
+    prev, new = W.serving_target(seed=71, batch=3), W.serving_target(seed=72, batch=3)
+    dp, dn = gb.upload(prev), gb.upload(new)
+    status = gb.new_status()
+    mask, depth = gb.gdn_tree_build_desc(dn["parent"], dn["node_offsets"], new.max_nodes, dev_status=status)
+    o, S = gb.gdn_tree_commit_verify(dp, dp["S0"], prev.max_nodes, 16, dn["q"], dn["k"], dn["v"], dn["g"],
+                                     dn["beta"], dn["node_offsets"], dn["parent"], mask, depth,
+                                     new.max_nodes, max_depth=16, out_dtype=torch.float32, dev_status=status)
+    torch.cuda.synchronize()
+    gb.check_status(status)
+    assert o.dtype == torch.float32
+    S_ref, o_ref = _reference(prev, new)
+    assert _rel(S.cpu().numpy(), S_ref) <= TOL_STATE
+    assert _rel(o.cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_wait_probe_times_out_and_the_chained_kernels_return():
+    prev, new = W.serving_target(seed=81, batch=3), W.serving_target(seed=82, batch=3)
+    o0, S0, status, _ = _run(prev, new)
+    gb.check_status(status)
+    try:
+        gb.gdn_test_set_wait_probe(2000)
+        o1, S1, status1, _ = _run(prev, new)
+        bits = int(status1.item())
+    finally:
+        gb.gdn_test_set_wait_probe(0)
+    assert bits == DEV_TIMEOUT
+    assert torch.equal(o1, o0) and torch.equal(S1, S0)
+    o2, S2, status2, _ = _run(prev, new)
+    gb.check_status(status2)
+    assert torch.equal(o2, o0) and torch.equal(S2, S0)
