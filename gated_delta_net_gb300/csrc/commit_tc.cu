@@ -16,13 +16,14 @@
 // next item's path data (keys, values, g, beta, node ids and their checks) is
 // prepared into a second buffer while thread 0 waits for the current state
 // tile's store, and the next tile is requested into L2.
-// Both contractions are GEMMs with a side as wide as the longest path (16, or 32
-// for longer paths) and run on tcgen05 with fp32 accumulation:
+// The contractions run on tcgen05 with fp32 accumulation, with a side as wide as
+// the longest path (P = 16, or 32 for longer paths):
+//     G  = K K^T       the path keys' Gram, for the chain coefficients
 //     W  = S0 K^T      M = 128 state rows, N = P path keys, K = 128
 //     U  = A K         M = 128 state rows, N = 128 columns, K = P path keys
 // where A[row][t] = e^(gamma_L - gamma_t) u_t[row].  The fp32 operands S0 and
 // A enter as bf16 hi + lo pairs (x = hi + lo to ~2^-17 relative) and the keys
-// are exact in bf16, so both products keep fp32 accuracy.  The chain solve for
+// are exact in bf16, so the products keep fp32 accuracy.  The chain solve for
 // u runs per state row in registers.  The state tile moves by TMA both ways and
 // is fully read before it is overwritten, so S_new may alias S0.
 #include <algorithm>
@@ -58,7 +59,7 @@ struct CommitCfg {
     static constexpr int kScal = 5 * P;                         // floats per buffer
     static constexpr int OFF_MISC = OFF_SCAL + kBufs * kScal * 4;  // tmem slot, bad path flags [2]
     static constexpr int OFF_BAR = OFF_MISC + 16;
-    static constexpr int kSmemBytes = OFF_BAR + 4 * 8;  // barriers: tile, W, U, probe (never arrived on)
+    static constexpr int kSmemBytes = OFF_BAR + 5 * 8;  // barriers: tile, W, U, probe (never arrived on), Gram
     static_assert(2 * kSmemBytes + 2048 <= 233472, "two blocks per SM");
 };
 
@@ -88,10 +89,6 @@ __device__ __forceinline__ int tile_index(int row, int col) {
 // bf16 K-major 128B-swizzled tile with `rows` rows (byte offset).
 __device__ __forceinline__ uint32_t sw128(int row, int k, int rows) {
     return (uint32_t)((k >> 6) * rows * 128 + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
-}
-
-__device__ __forceinline__ float bf16_at(const uint8_t *base, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
 }
 
 // The t-th set bit (0-based, ascending) of a multi-word mask row, or -1.
@@ -139,7 +136,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     if (tid == 0) {
-        for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
+        for (int k = 0; k < 5; ++k) mbar_init(&bar[k], 1);
         fence_mbar_init();
         s_bad[0] = s_bad[1] = 0;
     }
@@ -161,7 +158,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
     // test hook: a bounded wait on a barrier that nothing arrives on runs out,
     // and the block records GDN_DEV_TIMEOUT at exit; nothing else changes
     if (p.probe > 0 && tid == 0) ok = mbar_wait(&bar[3], 0, (uint32_t)p.probe);
-    uint32_t ph_tile = 0, ph_mma = 0;  // completed phases of the tile and MMA barriers
+    uint32_t ph_tile = 0, ph_mma = 0, ph_gram = 0;  // completed phases of the tile and MMA barriers
     int it = 0;                        // items committed by this block (path-data buffer = it & 1)
 
     struct Itm {
@@ -256,6 +253,7 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
                 vrow[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
             }
         }
+        fence_proxy_async_smem();  // the keys are also a tensor-core operand
     };
 
     int prepped = -1;  // the item whose path data is already in its buffer
@@ -297,21 +295,36 @@ commit_tc_kernel(const __grid_constant__ CUtensorMap tmS0, const __grid_constant
             for (int t = 0; t < L; ++t) fdec[t] = expf(acc - gam[t]);
         }
         __syncthreads();
-        // chain coefficients beta_t e^(gamma_t - gamma_s) (k_t . k_s): one warp per pair
-        if (!bad) {
-            for (int pr = warp; pr < L * (L - 1) / 2; pr += kT / 32) {
-                int t = 1, base = 0;
-                while (base + t <= pr) { base += t; ++t; }
-                const int s_ = pr - base;
-                float d = 0.f;
+        // chain coefficients beta_t e^(gamma_t - gamma_s) (k_t . k_s): the Gram K K^T of the
+        // path keys on the tensor cores (M = 128, of which rows past L read other shared
+        // memory and are ignored; N = P; into the P columns next to W), then lane t of
+        // warp 0 scales row t
+        if (!bad && L > 1) {
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16_f32(128, kMaxPath);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = lane * 4 + e;
-                    d = fmaf(bf16_at(keys, sw128(t, m, kMaxPath)), bf16_at(keys, sw128(s_, m, kMaxPath)), d);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t d = smem_desc(smem_u32(keys + (ks >> 2) * (kMaxPath * 128) + (ks & 3) * 32), 16, 1024, 2);
+                    mma_bf16(tmem + kMaxPath, d, d, id, ks > 0);
                 }
-                d = warp_sum(d);
-                if (lane == 0) coef[t * kMaxPath + s_] = bet[t] * expf(gam[t] - gam[s_]) * d;
+                mma_commit(&bar[4]);
             }
+            if (warp == 0) {
+                ok = mbar_wait(&bar[4], ph_gram & 1) && ok;
+                tc_fence_after();
+                uint32_t gv[32];  // columns past P are not read
+                tmem_ld32_nowait(tmem + kMaxPath, gv);
+                tmem_wait_ld_into(gv);
+                if (lane < L) {
+                    const float bt = bet[lane], gt = gam[lane];
+#pragma unroll
+                    for (int s_ = 0; s_ < kMaxPath - 1; ++s_)
+                        if (s_ < lane) coef[lane * kMaxPath + s_] = bt * expf(gt - gam[s_]) * __uint_as_float(gv[s_]);
+                }
+                tc_fence_before();
+            }
+            ++ph_gram;
         }
 
         // the state tile: row, columns 64 half .. 64 half + 63 into registers
