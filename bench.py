@@ -360,6 +360,7 @@ def run_ours(args, rank, world, local_rank):
     gb.check_status(status)
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     verify_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    commit_ms = [e[3].elapsed_time(e[1]) for e in evs]
     total_s = reduce_max(sum(step_ms) / 1e3, dev)
     value = job_throughput(T, args.steps, total_s, world)
     ms_per_step = total_s * 1e3 / args.steps
@@ -468,6 +469,8 @@ def run_ours(args, rank, world, local_rank):
     hbm_gbs, bf16_tf, peak_kind = load_peaks()
     vbytes = verify_bytes(tb)
     v_s = statistics.mean(verify_ms) / 1e3
+    cbytes = commit_bytes(tb)
+    c_s = statistics.mean(commit_ms) / 1e3
     achieved = vbytes / v_s / 1e9
     kernel = dominant_kernel(tb)
     traffic = None
@@ -491,6 +494,10 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": vbytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "commit_only": {"kernel": commit_kernel(tb), "us_per_launch": c_s * 1e6,
+                        "us_median": statistics.median(commit_ms) * 1e3,
+                        "achieved_gbs": cbytes / c_s / 1e9, "frac": cbytes / c_s / 1e9 / hbm_gbs,
+                        "algorithmic_bytes_per_launch": cbytes},
         "verify_only": {"us_per_launch": v_s * 1e6,
                         "us_median": statistics.median(verify_ms) * 1e3,
                         "us_max": max(verify_ms) * 1e3, "node_tokens_per_s": T / v_s,
@@ -558,6 +565,14 @@ def bench_workload(args):
         tb.max_depth_bound = 0
         tb.name += "_nobound"
     return tb
+
+
+def commit_kernel(tb) -> str:
+    """The commit kernel the library dispatches to for the declared path bound (the
+    workloads' max_path is their declared depth; rule of include/gdn_tree.h)."""
+    if TC_READY and tb.qkv_dtype == "bf16" and tb.d_k == 128 and tb.d_v == 128 and 1 <= tb.max_depth_bound <= 32:
+        return "commit_tc"
+    return "commit_simt"
 
 
 def dominant_kernel(tb) -> str:

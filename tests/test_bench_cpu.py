@@ -107,19 +107,20 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.source_sha(["a.cu"]) != h1
 
 
-@pytest.mark.parametrize("depth,size,workload,kernel", [
-    (16, 128, "serving_b64_n128", "verify_tc"),
-    (16, 256, "serving_b64_n256", "verify_wide"),
-    (32, 128, "deep_b64_n128_d32", "verify_wide"),
-    (64, 128, "deep_b64_n128_d64", "verify_wide"),
-    (0, 128, "serving_b64_n128_nobound", "verify_simt"),
+@pytest.mark.parametrize("depth,size,workload,kernel,commit", [
+    (16, 128, "serving_b64_n128", "verify_tc", "commit_tc"),
+    (16, 256, "serving_b64_n256", "verify_wide", "commit_tc"),
+    (32, 128, "deep_b64_n128_d32", "verify_wide", "commit_tc"),
+    (64, 128, "deep_b64_n128_d64", "verify_wide", "commit_simt"),
+    (0, 128, "serving_b64_n128_nobound", "verify_simt", "commit_simt"),
 ])
-def test_bench_workload_and_kernel(depth, size, workload, kernel):
+def test_bench_workload_and_kernel(depth, size, workload, kernel, commit):
     import argparse
     args = argparse.Namespace(depth=depth, batch=64, tree_size=size)
     tb = bench.bench_workload(args)
     assert tb.name == workload
     assert bench.dominant_kernel(tb) == kernel
+    assert bench.commit_kernel(tb) == commit
     assert tb.max_nodes == size
     # the declared depth bound holds for every tree, and deep workloads reach past 16
     depth_of = np.ones(tb.total_nodes, np.int64)
